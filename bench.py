@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Throughput of the speculative-sampling verification hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: `spec_sample_draft`
+(draw the K draft tokens of every sequence from the adjusted draft rows) and
+`spec_verify` (accept tests, residual / bonus draw) -- one kernel launch each.
+Metric: vocabulary rows processed per second (rows read from HBM by the two
+kernels), with the achieved HBM GB/s of the dominant kernel against the
+measured copy bandwidth as the roofline.
+
+Input sets: three device-resident sets of the workload rotate (together larger
+than L2).  Step j draws the tokens of set (j+1) % 3 and verifies set j % 3 with
+the tokens drawn one step earlier, so no kernel reads rows that the previous
+kernel left in L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no
+collective on the data path); timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "verify vocab-rows/s and achieved HBM GB/s (% of GB300 peak) on 1 GPU"
+NSETS = 3
+
+
+def rows_per_step(w):
+    """(sample_draft rows, verify rows) read from HBM per step."""
+    B, K = w["B"], w["K"]
+    return B * K, B * (K + 1 if w["greedy"] else 2 * K + 1)
+
+
+def esize(w):
+    return 2 if w["dtype"] == "bf16" else 4
+
+
+def workload_desc(name, w):
+    cfg = workloads.CONFIGS[name]
+    return "%s: %s, Zipf+Gaussian synthetic logits" % (name, cfg.describe()) if cfg.kind == "zipf" \
+        else "%s: %s, Gaussian synthetic logits" % (name, cfg.describe())
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+BAD_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+
+
+# ---------------------------------------------------------------------------
+# oracle on the host cores (cpu_baseline leg and the reference arm)
+
+def oracle_step(w, seqs, threads):
+    """Oracle sample_draft + verify over the sequence subset `seqs` on `threads` host
+    threads (ctypes releases the GIL).  Returns the vocab rows processed."""
+    import oracle
+    prm = dict(temperature=w["temperature"], top_k=w["top_k"], top_p=w["top_p"], greedy=w["greedy"])
+    parts = np.array_split(np.asarray(seqs), max(1, min(threads, len(seqs))))
+
+    def work(idx):
+        if len(idx) == 0:
+            return
+        sd = oracle.sample_draft(w["draft"][idx], w["u_draft"][idx], **prm)
+        oracle.verify(w["target"][idx], w["draft"][idx], sd["tokens"], w["u_verify"][idx], **prm)
+
+    ts = [threading.Thread(target=work, args=(p,)) for p in parts]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    rs, rv = rows_per_step(dict(w, B=len(seqs)))
+    return rs + rv
+
+
+def cpu_baseline(w, threads):
+    """Time the oracle as it stands on one full batch of the workload (bounded sample)."""
+    import oracle
+    oracle.build()
+    seqs = np.arange(w["B"])
+    t0 = time.perf_counter()
+    rows = oracle_step(w, seqs, threads)
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "sample": "one step over all %d sequences of the workload (%d vocab rows), "
+                      "%d host threads, %.2f s wall" % (w["B"], rows, threads, dt)}
+
+
+def run_reference(args, name):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = workloads.make(name)
+    threads = os.cpu_count() or 1
+    # size each step so the whole run stays within a few minutes
+    t0 = time.perf_counter()
+    oracle_step(w, np.arange(min(threads, w["B"])), threads)
+    t_one = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    nseq = min(w["B"], threads) if t_one <= budget else 1
+    seqs = np.arange(nseq)
+    for _ in range(args.warmup):
+        oracle_step(w, seqs, threads)
+    rows = 0
+    t0 = time.perf_counter()
+    for j in range(args.steps):
+        rows += oracle_step(w, (seqs + j * nseq) % w["B"], threads)
+    dt = time.perf_counter() - t0
+    val = rows / dt
+    cfg = dict(workload=workload_desc(name, w), input_dtype=w["dtype"], global_batch=w["B"],
+               vocab=w["V"], draft_len=w["K"], parallelism="host threads")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": val, "unit": "rows/s", "cores": threads, "kind": "oracle",
+                             "sample": "%d sequence(s) of the workload per step" % nseq},
+            "e2e": {"value": val, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+
+def run_gpu(args, name):
+    import torch
+    import speculative_sampling_verification_spec_gb300 as sv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    sv.binding.lib()
+
+    # inputs: NSETS seeded sets per rank (rank offsets the seed: weak scaling)
+    base = workloads.CONFIGS[name]
+    sets = []
+    host_first = None
+    for s in range(NSETS):
+        w = workloads.make(name, seed=base.seed + 1000 * rank + 17 * s)
+        if s == 0:
+            host_first = w
+        conv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)) if w["dtype"] == "bf16" \
+            else torch.from_numpy
+        sets.append(dict(tgt=conv(w["target"]).to(dev), drf=conv(w["draft"]).to(dev),
+                         ud=torch.from_numpy(w["u_draft"]).to(dev),
+                         uv=torch.from_numpy(w["u_verify"]).to(dev),
+                         tok=torch.zeros((w["B"], w["K"]), dtype=torch.int32, device=dev)))
+    w = host_first
+    prm = dict(temperature=w["temperature"], top_k=w["top_k"], top_p=w["top_p"], greedy=w["greedy"])
+    B, K, V = w["B"], w["K"], w["V"]
+    dt_code = sv.SPEC_BF16 if w["dtype"] == "bf16" else sv.SPEC_F32
+    ws_v = torch.zeros(sv.spec_verify_workspace_size(B, K, V, dt_code, w["greedy"]), dtype=torch.uint8, device=dev)
+    ws_s = torch.zeros(sv.spec_sample_draft_workspace_size(B, K, V, dt_code, w["greedy"]), dtype=torch.uint8, device=dev)
+    out_t = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def sample(s):
+        st = sets[s]
+        sv.spec_sample_draft(st["drf"], None if w["greedy"] else st["ud"], out_tokens=st["tok"], ws=ws_s, **prm)
+
+    def verify(s):
+        st = sets[s]
+        sv.spec_verify(st["tgt"], None if w["greedy"] else st["drf"], st["tok"],
+                       None if w["greedy"] else st["uv"], out_tokens=out_t, out_num_accepted=out_n,
+                       ws=ws_v, **prm)
+
+    for s in range(NSETS):
+        sample(s)
+    for j in range(args.warmup):
+        sample((j + 1) % NSETS)
+        verify(j % NSETS)
+    torch.cuda.synchronize(dev)
+
+    rs, rv = rows_per_step(w)
+    es = esize(w)
+    bytes_s, bytes_v = rs * V * es, rv * V * es
+
+    def timed(steps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        n0 = sv.spec_launch_count()
+        clk = ClockSampler(local)
+        clk.start()
+        time.sleep(0.25)  # let the sampler come up before the timed region
+        t_host = time.perf_counter()
+        for j in range(steps):
+            e0, e1, e2 = ev[j]
+            e0.record(stream)
+            sample((j + 1) % NSETS)
+            e1.record(stream)
+            verify(j % NSETS)
+            e2.record(stream)
+        torch.cuda.synchronize(dev)
+        t_host = time.perf_counter() - t_host
+        clocks = clk.stop()
+        launches = sv.spec_launch_count() - n0
+        t_s = [ev[j][0].elapsed_time(ev[j][1]) for j in range(steps)]
+        t_v = [ev[j][1].elapsed_time(ev[j][2]) for j in range(steps)]
+        total_ms = ev[0][0].elapsed_time(ev[-1][2])
+        return dict(total_ms=total_ms, t_s=t_s, t_v=t_v, launches=launches, clocks=clocks, t_host=t_host)
+
+    r = timed(args.steps)
+    note = None
+    if set(r["clocks"]["reasons"]) & BAD_REASONS:
+        note = "first measurement saw %s; re-measured once" % sorted(set(r["clocks"]["reasons"]) & BAD_REASONS)
+        r = timed(args.steps)
+    total_ms = r["total_ms"]
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    rows_step = rs + rv
+    value = world * rows_step * args.steps / (total_ms / 1e3)
+    avg_v = sum(r["t_v"]) / len(r["t_v"])
+    avg_s = sum(r["t_s"]) / len(r["t_s"])
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_v / (avg_v / 1e3) / 1e9
+
+    # end to end through the public API: host (pinned) inputs -> device -> outputs -> host
+    e2e_steps = max(3, min(args.steps, 50))
+    conv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)) if w["dtype"] == "bf16" \
+        else torch.from_numpy
+    h_t = conv(w["target"]).pin_memory()
+    h_d = conv(w["draft"]).pin_memory()
+    h_ud = torch.from_numpy(w["u_draft"]).pin_memory()
+    h_uv = torch.from_numpy(w["u_verify"]).pin_memory()
+    h_out_t = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h_out_n = torch.empty((B,), dtype=torch.int32).pin_memory()
+    d_t, d_d = torch.empty_like(h_t, device=dev), torch.empty_like(h_d, device=dev)
+    d_ud, d_uv = torch.empty_like(h_ud, device=dev), torch.empty_like(h_uv, device=dev)
+    d_tok = torch.empty((B, K), dtype=torch.int32, device=dev)
+    h2d = (h_t.numel() * h_t.element_size() + (0 if w["greedy"] else
+           h_d.numel() * h_d.element_size() + h_ud.numel() * 8 + h_uv.numel() * 8))
+    if w["greedy"]:
+        h2d += h_d.numel() * h_d.element_size()  # greedy drafts are still drawn from the draft rows
+    d2h = h_out_t.numel() * 4 + h_out_n.numel() * 4
+
+    def e2e_step():
+        d_t.copy_(h_t, non_blocking=True)
+        d_d.copy_(h_d, non_blocking=True)
+        if not w["greedy"]:
+            d_ud.copy_(h_ud, non_blocking=True)
+            d_uv.copy_(h_uv, non_blocking=True)
+        sv.spec_sample_draft(d_d, None if w["greedy"] else d_ud, out_tokens=d_tok, ws=ws_s, **prm)
+        sv.spec_verify(d_t, None if w["greedy"] else d_d, d_tok, None if w["greedy"] else d_uv,
+                       out_tokens=out_t, out_num_accepted=out_n, ws=ws_v, **prm)
+        h_out_t.copy_(out_t, non_blocking=True)
+        h_out_n.copy_(out_n, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_val = world * rows_step * e2e_steps / e2e_s
+
+    base_cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base_cpu = cpu_baseline(host_first, os.cpu_count() or 1)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_desc(name, w), "input_dtype": w["dtype"],
+                       "global_batch": B * world, "vocab": V, "draft_len": K,
+                       "rows_per_step": rows_step, "step": "spec_sample_draft + spec_verify",
+                       "l2": "%d rotating device input sets (%.0f MB) > L2; step j samples set j+1, verifies set j"
+                             % (NSETS, NSETS * (bytes_v) / 1e6),
+                       "parallelism": "dp%d (independent batches)" % world},
+            "gbs": (bytes_s + bytes_v) * world / (ms_step / 1e3) / 1e9,
+            "kernels": {"spec_verify": {"avg_us": avg_v * 1e3, "rows": rv, "bytes": bytes_v,
+                                        "gbs": achieved, "rows_per_s": rv / (avg_v / 1e3)},
+                        "spec_sample_draft": {"avg_us": avg_s * 1e3, "rows": rs, "bytes": bytes_s,
+                                              "gbs": bytes_s / (avg_s / 1e3) / 1e9,
+                                              "rows_per_s": rs / (avg_s / 1e3)}},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "spec_rows_kernel (spec_verify)", "peak_kind": peak_kind},
+            "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
+            "gpu_launches": int(r["launches"]),
+            "clocks": {k: r["clocks"][k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+        }
+        if note:
+            line["clocks"]["note"] = note
+        if base_cpu is not None:
+            line["cpu_baseline"] = base_cpu
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="c5", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args, args.workload)
+    return run_gpu(args, args.workload)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,169 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 speculative-sampling verification library
+ * (libspecverify.so, CUDA kernels for sm_103a).
+ *
+ * The operation is the verification step of speculative sampling as the pages
+ * state it:
+ *   - "Speculative Decoding" (roadtointelligence.com), section "Draft, then
+ *     verify": a draft proposes K tokens, the target scores all K positions
+ *     plus one more in one pass, each draft token x is kept with probability
+ *     min(1, target(x)/draft(x)) left to right, the first rejection is
+ *     replaced by a draw from the normalised max(0, target - draft) and the
+ *     rest of the draft is discarded; if every draft token is kept, one more
+ *     token is drawn from the target's extra position.  Each round emits
+ *     between 1 and K+1 tokens.
+ *   - "Accelerating Large Language Model Decoding with Speculative Sampling"
+ *     (paperlayer.ai summary), section "Speculative Sampling", bullets
+ *     "Modified Rejection Sampling": nucleus, top-k and temperature are
+ *     applied before rejection sampling; the FDE Interviews breakdown of the
+ *     same paper, section "01 The paper in one minute", adds greedy decoding.
+ *   - "Speculative decoding: how to run large models faster" (ai-trend.me),
+ *     section "How it works": argmax, top-k, nucleus and temperature are each
+ *     sampling from an adjusted distribution.
+ *
+ * Conventions (all entry points):
+ *   - Every buffer is owned by the caller.  Device pointers must stay valid
+ *     until the work queued on params->stream has finished.  The library
+ *     allocates no device memory per call: it needs a caller-provided
+ *     workspace (see *_workspace_size) whose contents need no initialisation
+ *     (per-call tags mark stale values).  Calls that share one workspace must
+ *     not overlap in time on the GPU.
+ *   - Calls are asynchronous on params->stream (a cudaStream_t; NULL = the
+ *     legacy default stream).  Argument errors are detected on the host,
+ *     returned synchronously, and nothing is launched.
+ *   - Errors found on the device never trap: the affected sequence (verify)
+ *     or row (sample_draft) gets -1 in its outputs, and, when params->status
+ *     is not NULL, the first error code is stored there (atomically, from 0;
+ *     the caller zeroes it).  When several sequences fail with different
+ *     codes, which code is stored is unspecified.
+ *   - Inputs are never modified.
+ *
+ * Readings where the pages are silent (the same ones the fp64 test oracle
+ * takes): the accept test is  u_t * drf_t(d_t) < tgt_t(d_t)  (no division,
+ * so a draft probability of 0 accepts iff the target's is positive); draws walk
+ * the vocabulary in ascending index order and return the smallest x with
+ * u * R < sum_{y<=x} r(y), or, if rounding leaves none, the last x with
+ * r(x) > 0; a zero residual mass draws from the target row instead; top-k and
+ * top-p order tokens by raw logit (descending, ties to the lower index), apply
+ * top-k first, then keep the shortest prefix whose mass reaches top_p
+ * (crossing token included); -inf logits have probability 0; NaN or +inf
+ * logits, or a row with no finite logit, are errors.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1,  /* host: bad shape, pointer, stride, parameter or workspace */
+  SPEC_ERR_CUDA = 2,         /* host: a CUDA runtime call failed (launch, attribute) */
+  SPEC_ERR_NONFINITE = 3,    /* device: NaN or +inf logit, or no finite logit, in a row read */
+  SPEC_ERR_TOKEN_RANGE = 4,  /* device: a draft token outside [0, V) */
+  SPEC_ERR_TIMEOUT = 5,      /* device: a bounded wait on an asynchronous copy ran out */
+  SPEC_ERR_UNSUPPORTED = 6   /* host: V too large for one row per thread-block cluster */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+typedef struct {
+  int32_t B;                 /* sequences, >= 0 */
+  int32_t K;                 /* draft tokens per sequence, >= 1 */
+  int32_t V;                 /* vocabulary size, >= 1 */
+  int32_t dtype;             /* spec_dtype of both logit tensors */
+  /* Strides in ELEMENTS.  Row (b, t) of the target starts at
+   * target_logits + b*target_seq_stride + t*target_row_stride; likewise for the
+   * draft.  Any non-negative values are accepted (0 repeats rows); rows whose
+   * start is 16-byte aligned take the bulk-copy path, others a plain-load path. */
+  int64_t target_seq_stride, target_row_stride;
+  int64_t draft_seq_stride, draft_row_stride;
+  float temperature;         /* > 0 and finite unless greedy */
+  int32_t top_k;             /* >= 0; 0 or >= V = no top-k */
+  float top_p;               /* in (0, 1]; 1 = no nucleus filter */
+  int32_t greedy;            /* nonzero: argmax special case (uniforms and draft rows unused) */
+  void* stream;              /* cudaStream_t */
+  int32_t* status;           /* optional device int32[1]: first device-detected error */
+  void* workspace;           /* device, 256-byte aligned, any contents */
+  size_t workspace_bytes;
+} spec_params;
+
+/* Per-row record kept in the workspace (read back by spec_read_row_stats).
+ * For every row the kernels read: zf = sum over kept x of 2^((l_x - m) * log2(e)/T),
+ * the normaliser of the adjusted distribution relative to the row max m;
+ * p_tok = adjusted probability of the sequence's draft token at this row
+ * (verify, rows t < K; 0 otherwise); kept x satisfy l_x > tau_val, or
+ * l_x == tau_val and x <= tau_idx; list_len >= 0 when the kept set (index order)
+ * is stored in the workspace; flags: bit 0 non-finite row, bit 1 token out of
+ * range, bit 2 timeout.  token = the drawn token (sample_draft only). */
+typedef struct {
+  double zf;
+  double p_tok;
+  float m;
+  float tau_val;
+  int32_t tau_idx;
+  int32_t argmax;
+  int32_t list_len;
+  int32_t flags;
+  int32_t token;
+  int32_t pad_;
+} spec_row_stat;
+
+/* Workspace bytes spec_verify needs for these parameters (0 if they are invalid).
+ * Rows per sequence: 2K+1 (sampling) or K+1 (greedy). */
+size_t spec_verify_workspace_size(const spec_params* params);
+
+/* Workspace bytes spec_sample_draft needs (0 if the parameters are invalid). */
+size_t spec_sample_draft_workspace_size(const spec_params* params);
+
+/* Verification step, one call for B independent sequences.
+ *   target_logits     device, [B, K+1, V] rows (strides above), dtype
+ *   draft_logits      device, [B, K, V] rows; may be NULL when greedy
+ *   draft_tokens      device int32 [B, K], contiguous
+ *   uniforms          device fp64 [B, K+1], contiguous: column t < K drives the
+ *                     accept test at t, column K the single final draw (residual
+ *                     or bonus); may be NULL when greedy
+ *   out_tokens        device int32 [B, K+1]: the accepted draft tokens, then the
+ *                     replacement or bonus token, then -1 padding
+ *   out_num_accepted  device int32 [B]: accepted draft tokens n in [0, K]
+ *                     (n+1 tokens emitted), or -1 for a sequence with an error */
+spec_status spec_verify(const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, const double* uniforms,
+                        const spec_params* params, int32_t* out_tokens,
+                        int32_t* out_num_accepted);
+
+/* Draw the K draft tokens of each sequence from the adjusted draft distribution
+ * (same temperature / top-k / top-p / greedy as verification), one inverse-CDF
+ * draw per row in index order ("Speculative Decoding", section "Draft, then
+ * verify", step 1).  In real decoding drafting is sequential and each call
+ * draws K = 1 token per sequence; any K is accepted.
+ *   draft_logits  device [B, K, V] rows (draft strides)
+ *   uniforms      device fp64 [B, K], contiguous; may be NULL when greedy
+ *   out_tokens    device int32 [B, K] (-1 for a row with an error)
+ * The target fields of params are ignored. */
+spec_status spec_sample_draft(const void* draft_logits, const double* uniforms,
+                              const spec_params* params, int32_t* out_tokens);
+
+/* Copy the per-row records of the last call made with this workspace and these
+ * parameters into host memory: rows ordered by sequence, then target rows
+ * 0..K followed by draft rows 0..K-1 (verify; greedy: target rows only), or
+ * draft rows 0..K-1 (sample_draft, is_verify = 0).  Synchronises params->stream.
+ * Returns SPEC_ERR_INVALID_ARG if max_rows is smaller than the row count. */
+spec_status spec_read_row_stats(const spec_params* params, int32_t is_verify,
+                                spec_row_stat* host_out, int64_t max_rows);
+
+/* Static description of a status code. */
+const char* spec_status_string(spec_status status);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t spec_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

@@ -1,0 +1,229 @@
+"""Python binding of libspecverify.so: argument marshalling only.
+
+Each function here has the name of the C entry point it calls (see
+include/spec_verify.h) and does nothing but turn torch CUDA tensors into
+pointers, strides and a stream handle.  Every step of the computation runs in
+the library's CUDA kernels; there is no CPU or PyTorch fallback, and a missing
+library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+SPEC_OK = 0
+SPEC_F32, SPEC_BF16 = 0, 1
+STATUS_NAMES = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_CUDA", 3: "SPEC_ERR_NONFINITE",
+                4: "SPEC_ERR_TOKEN_RANGE", 5: "SPEC_ERR_TIMEOUT", 6: "SPEC_ERR_UNSUPPORTED"}
+EXPORTED = ("spec_verify", "spec_sample_draft", "spec_verify_workspace_size",
+            "spec_sample_draft_workspace_size", "spec_read_row_stats", "spec_status_string",
+            "spec_launch_count")
+
+
+class SpecParams(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("target_seq_stride", ctypes.c_int64), ("target_row_stride", ctypes.c_int64),
+        ("draft_seq_stride", ctypes.c_int64), ("draft_row_stride", ctypes.c_int64),
+        ("temperature", ctypes.c_float), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float),
+        ("greedy", ctypes.c_int32),
+        ("stream", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class SpecRowStat(ctypes.Structure):
+    _fields_ = [
+        ("zf", ctypes.c_double), ("p_tok", ctypes.c_double), ("m", ctypes.c_float),
+        ("tau_val", ctypes.c_float), ("tau_idx", ctypes.c_int32), ("argmax", ctypes.c_int32),
+        ("list_len", ctypes.c_int32), ("flags", ctypes.c_int32), ("token", ctypes.c_int32),
+        ("pad_", ctypes.c_int32),
+    ]
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__("%s: %s (%s)" % (what, STATUS_NAMES.get(code, code), spec_status_string(code)))
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise FileNotFoundError(
+                    "libspecverify.so is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(_build.LIB)
+            P = ctypes.c_void_p
+            PP = ctypes.POINTER(SpecParams)
+            L.spec_verify.argtypes = [P, P, P, P, PP, P, P]
+            L.spec_verify.restype = ctypes.c_int
+            L.spec_sample_draft.argtypes = [P, P, PP, P]
+            L.spec_sample_draft.restype = ctypes.c_int
+            L.spec_verify_workspace_size.argtypes = [PP]
+            L.spec_verify_workspace_size.restype = ctypes.c_size_t
+            L.spec_sample_draft_workspace_size.argtypes = [PP]
+            L.spec_sample_draft_workspace_size.restype = ctypes.c_size_t
+            L.spec_read_row_stats.argtypes = [PP, ctypes.c_int32, P, ctypes.c_int64]
+            L.spec_read_row_stats.restype = ctypes.c_int
+            L.spec_status_string.argtypes = [ctypes.c_int]
+            L.spec_status_string.restype = ctypes.c_char_p
+            L.spec_launch_count.argtypes = []
+            L.spec_launch_count.restype = ctypes.c_uint64
+            _lib = L
+    return _lib
+
+
+def spec_status_string(code: int) -> str:
+    return lib().spec_status_string(int(code)).decode()
+
+
+def spec_launch_count() -> int:
+    return int(lib().spec_launch_count())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError("logits must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("spec_* calls take CUDA tensors (copy host data to the GPU first)")
+
+
+_ws_cache = {}
+
+
+def workspace(nbytes: int, device: torch.device) -> torch.Tensor:
+    """A zero-filled device workspace of at least nbytes, cached per device (the
+    kernels leave it reusable, so it is zeroed only when first allocated)."""
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def make_params(B, K, V, dtype, tgt_strides=(0, 0), drf_strides=(0, 0), temperature=1.0, top_k=0,
+                top_p=1.0, greedy=False, stream=None, status=None, ws=None) -> SpecParams:
+    return SpecParams(int(B), int(K), int(V), int(dtype), int(tgt_strides[0]), int(tgt_strides[1]),
+                      int(drf_strides[0]), int(drf_strides[1]), float(temperature), int(top_k),
+                      float(top_p), int(bool(greedy)), stream,
+                      None if status is None else status.data_ptr(),
+                      None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel())
+
+
+def _stream_handle(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def spec_verify_workspace_size(B, K, V, dtype, greedy=False) -> int:
+    p = make_params(B, K, V, dtype, greedy=greedy)
+    return int(lib().spec_verify_workspace_size(ctypes.byref(p)))
+
+
+def spec_sample_draft_workspace_size(B, K, V, dtype, greedy=False) -> int:
+    p = make_params(B, K, V, dtype, greedy=greedy)
+    return int(lib().spec_sample_draft_workspace_size(ctypes.byref(p)))
+
+
+def spec_verify(target, draft, draft_tokens, uniforms, *, temperature=1.0, top_k=0, top_p=1.0,
+                greedy=False, out_tokens=None, out_num_accepted=None, status=None, ws=None,
+                stream=None, B=None):
+    """target [B, K+1, V] and draft [B, K, V] CUDA logits (any element strides for the
+    first two dims, unit stride along V), draft_tokens [B, K] int32, uniforms [B, K+1]
+    float64.  Returns (out_tokens [B, K+1] int32, out_num_accepted [B] int32)."""
+    _check_cuda(target, draft, draft_tokens, uniforms)
+    K = draft_tokens.shape[1]
+    B = draft_tokens.shape[0] if B is None else B
+    V = target.shape[-1]
+    dt = _dtype_code(target)
+    if draft is not None and draft.dtype != target.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    if target.stride(-1) != 1 or (draft is not None and draft.stride(-1) != 1):
+        raise ValueError("logit rows must be contiguous along the vocabulary")
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    tstr = (target.stride(0), target.stride(1))
+    dstr = (draft.stride(0), draft.stride(1)) if draft is not None else (0, 0)
+    p = make_params(B, K, V, dt, tstr, dstr, temperature, top_k, top_p, greedy,
+                    _stream_handle(stream), status)
+    if ws is None:
+        ws = workspace(int(lib().spec_verify_workspace_size(ctypes.byref(p))), dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    tok = draft_tokens if draft_tokens.dtype == torch.int32 else draft_tokens.to(torch.int32)
+    u = uniforms
+    if u is not None and u.dtype != torch.float64:
+        raise TypeError("uniforms must be float64")
+    code = lib().spec_verify(_ptr(target), _ptr(draft), _ptr(tok.contiguous()),
+                             _ptr(None if u is None else u.contiguous()), ctypes.byref(p),
+                             _ptr(out_tokens), _ptr(out_num_accepted))
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_verify")
+    return out_tokens, out_num_accepted
+
+
+def spec_sample_draft(draft, uniforms, *, temperature=1.0, top_k=0, top_p=1.0, greedy=False,
+                      out_tokens=None, status=None, ws=None, stream=None):
+    """draft [B, K, V] CUDA logits, uniforms [B, K] float64 (None when greedy).
+    Returns out_tokens [B, K] int32."""
+    _check_cuda(draft, uniforms)
+    B, K, V = draft.shape[0], draft.shape[1], draft.shape[-1]
+    if draft.stride(-1) != 1:
+        raise ValueError("logit rows must be contiguous along the vocabulary")
+    dev = draft.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    p = make_params(B, K, V, _dtype_code(draft), (0, 0), (draft.stride(0), draft.stride(1)),
+                    temperature, top_k, top_p, greedy, _stream_handle(stream), status)
+    if ws is None:
+        ws = workspace(int(lib().spec_sample_draft_workspace_size(ctypes.byref(p))), dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    if uniforms is not None and uniforms.dtype != torch.float64:
+        raise TypeError("uniforms must be float64")
+    code = lib().spec_sample_draft(_ptr(draft), _ptr(None if uniforms is None else uniforms.contiguous()),
+                                   ctypes.byref(p), _ptr(out_tokens))
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_sample_draft")
+    return out_tokens
+
+
+def spec_read_row_stats(B, K, V, dtype, is_verify, ws, *, greedy=False, temperature=1.0, top_k=0,
+                        top_p=1.0, stream=None):
+    """Per-row records of the last call made with workspace `ws` (list of dicts)."""
+    p = make_params(B, K, V, dtype, temperature=temperature, top_k=top_k, top_p=top_p,
+                    greedy=greedy, stream=_stream_handle(stream), ws=ws)
+    R = (K + 1 if greedy else 2 * K + 1) if is_verify else K
+    n = B * R
+    arr = (SpecRowStat * max(n, 1))()
+    code = lib().spec_read_row_stats(ctypes.byref(p), int(bool(is_verify)), arr, n)
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_read_row_stats")
+    return [{f: getattr(arr[i], f) for f, _ in SpecRowStat._fields_ if f != "pad_"} for i in range(n)]

@@ -1,0 +1,241 @@
+"""Parity of the CUDA path (called through the C ABI) with the fp64 oracle.
+
+Bar: out_tokens and out_num_accepted bit-exact, excluding only sequences the
+oracle flags as having a uniform (or a top-p cumulative mass) within 1e-6 of a
+decision threshold; per-row normalisers and draft-token probabilities within
+1e-5 relative.  Flagged sequences are counted, and must stay rare.
+"""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+import oracle
+import workloads
+from _gpu import check_invariants, compare_verify, params_of, to_dev
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import speculative_sampling_verification_spec_gb300 as m
+    m.binding.lib()
+    return m
+
+
+def run_case(sv, w, check_stats=True, seqs=None, where="", max_flag_frac=0.1):
+    """GPU verify on all of w's sequences; oracle on `seqs` (default all).  At most
+    max_flag_frac of the compared sequences (and at least one) may be flagged."""
+    prm = params_of(w)
+    d = oracle.sample_draft(w["draft"], w["u_draft"], **prm)
+    assert d["status"] == oracle.OK
+    tokens = d["tokens"]
+    tgt, drf = to_dev(w["target"]), to_dev(w["draft"])
+    ws = sv.workspace(sv.spec_verify_workspace_size(w["B"], w["K"], w["V"], sv.SPEC_BF16 if w["dtype"] == "bf16" else sv.SPEC_F32, w["greedy"]), torch.device(DEV))
+    out_t, out_n = sv.spec_verify(tgt, drf, to_dev(tokens), to_dev(w["u_verify"]), ws=ws, **prm)
+    torch.cuda.synchronize()
+    gt, gn = out_t.cpu().numpy(), out_n.cpu().numpy()
+    check_invariants(gt, gn, tokens, w["K"], w["V"])
+    sel = np.arange(w["B"]) if seqs is None else np.asarray(seqs)
+    ref = oracle.verify(w["target"][sel], w["draft"][sel], tokens[sel], w["u_verify"][sel],
+                        with_stats=check_stats, **prm)
+    assert ref["status"] == oracle.OK
+    nflag = compare_verify(gt[sel], gn[sel], ref, where)
+    assert nflag <= max(1, int(max_flag_frac * len(sel))), "%s: %d flagged sequences" % (where, nflag)
+    if check_stats:
+        dt = sv.SPEC_BF16 if w["dtype"] == "bf16" else sv.SPEC_F32
+        rows = sv.spec_read_row_stats(w["B"], w["K"], w["V"], dt, True, ws, **prm)
+        R = w["K"] + 1 if w["greedy"] else 2 * w["K"] + 1
+        for bi, b in enumerate(sel):
+            for r in range(R):
+                g = rows[b * R + r]
+                o = ref["row_stats"][bi, r]
+                assert g["flags"] == 0
+                assert g["m"] == o[0], (where, b, r)
+                if not w["greedy"]:
+                    assert abs(g["zf"] - o[1]) <= 1e-5 * o[1], (where, b, r, g["zf"], o[1])
+                    if o[2] > 1e-300:
+                        assert abs(g["p_tok"] - o[2]) <= 1e-5 * o[2], (where, b, r, g["p_tok"], o[2])
+                    else:
+                        assert g["p_tok"] < 1e-30
+    return gt, gn, tokens
+
+
+SMALL = [
+    ("c1", {}),
+    ("c2", {}),
+    ("c3", dict(B=6, V=50001)),        # odd V: rows not 16-byte aligned (plain-load path)
+    ("c3", dict(B=3)),                 # full V = 128256
+    ("c4", dict(B=24)),                # full V = 50304, fp32 greedy
+    ("c4", dict(B=16, V=20011)),
+    ("c4_bf16", dict(B=24)),
+    ("c5", dict(B=3)),                 # full V = 256000
+    ("c5", dict(B=6, V=70003)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=["%s-%s" % (n, "-".join("%s%s" % kv for kv in k.items())) for n, k in SMALL])
+def test_verify_matches_oracle(sv, name, kw):
+    w = workloads.make(name, **kw)
+    run_case(sv, w, where=name)
+
+
+@pytest.mark.parametrize("name", ["c3", "c4", "c4_bf16", "c5"])
+def test_full_size_sampled_sequences(sv, name):
+    """The bench's launch configuration (full B, K, V); the oracle checks a sample."""
+    w = workloads.make(name)
+    B = w["B"]
+    seqs = sorted({0, 1, B // 3, (2 * B) // 3, B - 1})
+    run_case(sv, w, check_stats=True, seqs=seqs, where=name + "-full")
+
+
+@pytest.mark.parametrize("name,kw", [("c1", {}), ("c2", {}), ("c3", dict(B=4, V=60007)),
+                                     ("c5", dict(B=2)), ("c4", dict(B=8))])
+def test_sample_draft_matches_oracle(sv, name, kw):
+    w = workloads.make(name, **kw)
+    prm = params_of(w)
+    ref = oracle.sample_draft(w["draft"], w["u_draft"], **prm)
+    g = sv.spec_sample_draft(to_dev(w["draft"]), to_dev(w["u_draft"]), **prm).cpu().numpy()
+    ok = ref["flags"] == 0
+    assert np.array_equal(g[ok], ref["tokens"][ok])
+    assert (~ok).sum() <= max(1, ok.size // 10)
+
+
+def _custom(B, K, V, rng, scale=2.0, dtype="f32"):
+    tl = rng.normal(0, scale, (B, K + 1, V)).astype(np.float32)
+    dl = (tl[:, :K] + rng.normal(0, 1.0, (B, K, V))).astype(np.float32)
+    if dtype == "bf16":
+        tl, dl = workloads.to_bf16_bits(tl), workloads.to_bf16_bits(dl)
+    return dict(target=tl, draft=dl, u_draft=rng.random((B, K)), u_verify=rng.random((B, K + 1)),
+                B=B, K=K, V=V, dtype=dtype, temperature=1.0, top_k=0, top_p=1.0, greedy=False)
+
+
+@pytest.mark.parametrize("case", [
+    dict(V=1, K=1, B=3),
+    dict(V=7, K=1, B=40),
+    dict(V=3000, K=2, B=6, top_k=1000),               # top-k beyond the on-chip sort: tie-cut path
+    dict(V=3000, K=2, B=6, top_k=40, top_p=0.8),
+    dict(V=20000, K=2, B=4, top_k=2000, top_p=0.95),  # top-p inside a tie-cut top-k set
+    # huge nucleus (kept set beyond the stored list) over a near-flat row: each tail token
+    # holds ~2e-5 of the mass, so a top-p cut lands within 1e-6 of 0.9999 in ~10% of rows
+    dict(V=9000, K=3, B=24, top_p=0.9999, scale=0.5, max_flag_frac=0.75),
+    dict(V=5000, K=2, B=4, temperature=0.05),
+    dict(V=5000, K=2, B=4, temperature=5.0, top_p=0.5),
+    dict(V=4099, K=3, B=5, dtype="bf16", top_k=13, temperature=0.7),
+    dict(V=2048, K=4, B=8, greedy=True, dtype="bf16", scale=0.3),   # many exact ties
+])
+def test_edge_cases_match_oracle(sv, case):
+    rng = np.random.default_rng(zlib.crc32(repr(sorted(case.items())).encode()))
+    w = _custom(case["B"], case["K"], case["V"], rng, case.get("scale", 2.0), case.get("dtype", "f32"))
+    for k in ("temperature", "top_k", "top_p", "greedy"):
+        if k in case:
+            w[k] = case[k]
+    run_case(sv, w, where=str(case), max_flag_frac=case.get("max_flag_frac", 0.1))
+
+
+def test_ties_all_equal_logits_cut_by_index(sv):
+    B, K, V = 3, 2, 3000
+    w = dict(target=np.zeros((B, K + 1, V), np.float32), draft=np.zeros((B, K, V), np.float32),
+             u_draft=np.random.default_rng(1).random((B, K)),
+             u_verify=np.random.default_rng(2).random((B, K + 1)),
+             B=B, K=K, V=V, dtype="f32", temperature=1.0, top_k=7, top_p=1.0, greedy=False)
+    gt, gn, _ = run_case(sv, w, where="flat-topk")
+    assert np.all(gt[np.arange(B), gn] < 7)
+    # every token holds 1/V of the mass; top_p = 0.3123 keeps ceil(0.3123 V) tokens, and the
+    # crossing (937/3000 = 0.31233) stays clear of the 1e-6 band around top_p
+    w["top_k"], w["top_p"] = 0, 0.3123
+    gt, gn, _ = run_case(sv, w, where="flat-topp")
+    assert np.all(gt[np.arange(B), gn] < 937)
+
+
+def test_neg_inf_entries_and_layouts(sv):
+    rng = np.random.default_rng(31)
+    B, K, V = 5, 3, 1500
+    w = _custom(B, K, V, rng)
+    w["target"][:, :, ::3] = -np.inf
+    w["draft"][:, :, 1::5] = -np.inf
+    w["top_k"] = 30
+    run_case(sv, w, where="-inf")
+    # repeated rows through stride 0, and a padded row stride
+    prm = params_of(w)
+    one_t = to_dev(w["target"][:1])
+    one_d = to_dev(w["draft"][:1])
+    tgt = one_t.expand(B, K + 1, V)
+    drf = one_d.expand(B, K, V)
+    d = oracle.sample_draft(w["draft"][:1], w["u_draft"][:1], **prm)["tokens"].repeat(B, 0)
+    out_t, out_n = sv.spec_verify(tgt, drf, to_dev(d), to_dev(w["u_verify"]), **prm)
+    ref = oracle.verify(w["target"][:1], w["draft"][:1], d, w["u_verify"],
+                        tgt_strides=(0, V), drf_strides=(0, V), B=B, **prm)
+    compare_verify(out_t.cpu().numpy(), out_n.cpu().numpy(), ref, "stride0")
+    pad_t = torch.zeros(B, K + 1, V + 13, device=DEV)[:, :, :V]
+    pad_t.copy_(to_dev(w["target"]))
+    pad_d = torch.zeros(B, K, V + 13, device=DEV)[:, :, :V]
+    pad_d.copy_(to_dev(w["draft"]))
+    d = oracle.sample_draft(w["draft"], w["u_draft"], **prm)["tokens"]
+    out_t, out_n = sv.spec_verify(pad_t, pad_d, to_dev(d), to_dev(w["u_verify"]), **prm)
+    ref = oracle.verify(w["target"], w["draft"], d, w["u_verify"], **prm)
+    compare_verify(out_t.cpu().numpy(), out_n.cpu().numpy(), ref, "padded")
+
+
+def test_errors_reported_per_sequence(sv):
+    rng = np.random.default_rng(12)
+    B, K, V = 6, 2, 300
+    tl = rng.normal(0, 1, (B, K + 1, V)).astype(np.float32)
+    dl = rng.normal(0, 1, (B, K, V)).astype(np.float32)
+    d = rng.integers(0, V, (B, K)).astype(np.int32)
+    u = rng.random((B, K + 1))
+    tl[1, 2, 3] = np.nan
+    dl[2, 0, 5] = np.inf
+    tl[3, 0, :] = -np.inf
+    d[4, 1] = V
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out_t, out_n = sv.spec_verify(to_dev(tl), to_dev(dl), to_dev(d), to_dev(u), status=status)
+    ref = oracle.verify(tl, dl, d, u)
+    gn, gt = out_n.cpu().numpy(), out_t.cpu().numpy()
+    np.testing.assert_array_equal(gn, ref["num_accepted"])
+    for b in (1, 2, 3, 4):
+        assert gn[b] == -1 and np.all(gt[b] == -1)
+    assert int(status.item()) in (3, 4)
+    compare_verify(gt[[0, 5]], gn[[0, 5]], {k: v[[0, 5]] if k != "status" else v for k, v in ref.items()})
+
+
+def test_repeatable_bit_for_bit(sv):
+    w = workloads.make("c3", B=8, V=30011)
+    prm = params_of(w)
+    d = to_dev(oracle.sample_draft(w["draft"], w["u_draft"], **prm)["tokens"])
+    tgt, drf, u = to_dev(w["target"]), to_dev(w["draft"]), to_dev(w["u_verify"])
+    outs = [tuple(x.cpu().numpy().copy() for x in sv.spec_verify(tgt, drf, d, u, **prm)) for _ in range(3)]
+    for o in outs[1:]:
+        assert np.array_equal(o[0], outs[0][0]) and np.array_equal(o[1], outs[0][1])
+
+
+def test_worked_example_distribution_on_gpu(sv):
+    """"Speculative Decoding" (roadtointelligence.com), "Why the output doesn't change":
+    acceptance 0.8 and emitted words in the target's proportions, not the draft's."""
+    tgt_p = np.array([0.5, 0.25, 0.15, 0.10])
+    drf_p = np.array([0.3, 0.4, 0.2, 0.1])
+    lt, ld = np.log(tgt_p).astype(np.float32), np.log(drf_p).astype(np.float32)
+    B = 200_000
+    rng = np.random.default_rng(77)
+    tp = oracle.row_probs(lt)[0]
+    dp = oracle.row_probs(ld)[0]
+    d = rng.choice(4, size=(B, 1), p=dp).astype(np.int32)
+    u = rng.random((B, 2))
+    tgt = torch.from_numpy(np.stack([lt, lt])).to(DEV).unsqueeze(0).expand(B, 2, 4)
+    drf = torch.from_numpy(ld[None]).to(DEV).unsqueeze(0).expand(B, 1, 4)
+    out_t, out_n = sv.spec_verify(tgt, drf, to_dev(d), to_dev(u))
+    gt, gn = out_t.cpu().numpy(), out_n.cpu().numpy()
+    acc = (gn == 1).mean()
+    assert abs(acc - 0.8) < 4 * math.sqrt(0.16 / B)
+    counts = np.bincount(gt[:, 0], minlength=4)
+    assert stats.chisquare(counts, B * tp).pvalue > 1e-3
+    assert stats.chisquare(counts, B * dp).pvalue < 1e-12
+    ref = oracle.verify(np.stack([lt, lt])[None], ld[None, None], d, u, tgt_strides=(0, 4),
+                        drf_strides=(0, 4), B=B)
+    compare_verify(gt, gn, ref, "worked-example")
