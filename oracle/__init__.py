@@ -59,8 +59,9 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = ctypes.CDLL(_LIB)
+            # ORACLE_LIB lets the mutation tests load a deliberately broken copy
+            path = os.environ.get("ORACLE_LIB") or build()
+            L = ctypes.CDLL(path)
             P = ctypes.c_void_p
             L.oracle_row_probs.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                            ctypes.c_int32, ctypes.c_float, ctypes.c_int32,

@@ -215,6 +215,7 @@ struct Slot {  // per-CTA values published to the cluster
 struct alignas(128) Scratch {
   uint64_t bar[kStages];
   Slot slot[2];
+  Slot mirror[kMaxCluster];  // local copy of every rank's slot after an exchange
   // block-level reduction scratch
   float wf[kWarps];
   int32_t wi[kWarps];
@@ -242,6 +243,7 @@ struct SortBuf {
 constexpr size_t kSortBufBytes = kCap * (sizeof(unsigned long long) + sizeof(double));
 // scratch + a 64 KB slice must leave room for three CTAs in an SM's 228 KB
 static_assert(sizeof(Scratch) <= 8192, "shared scratch grew past its budget");
+static_assert(sizeof(Slot) % sizeof(uint32_t) == 0, "slots are copied as 32-bit words");
 
 // ---------------------------------------------------------------------------
 // warp / block helpers
@@ -296,25 +298,34 @@ __device__ double block_excl_scan_d(double v, double* total, Scratch& sm) {
 }
 
 // Iterate a warp's contiguous segment of n elements held as N-element vectors.
-// The loop is warp-uniform: f(x, first_elem, nvalid) runs on every lane each
-// iteration (nvalid = 0 for lanes past the end, whose x is -inf).
-template <int N, typename Load, typename F>
+// One iteration = 32 consecutive vectors, one per lane.  The loop is
+// warp-uniform: f(x, first_elem, nvalid) runs on every lane each iteration
+// (nvalid = 0 for lanes past the end, whose x is -inf).  U iterations' loads are
+// issued together before any is processed (memory-level parallelism for global
+// loads); the iterations themselves, and their order, do not depend on U.
+template <int N, int U = 1, typename Load, typename F>
 __device__ __forceinline__ void for_warp_segment(int n, int warp, int lane, Load load, F f) {
   const int nvec = (n + N - 1) / N;
   const int vpw = (nvec + kWarps - 1) / kWarps;
   const int vb = min(nvec, warp * vpw), ve = min(nvec, vb + vpw);
-  for (int base = vb; base < ve; base += 32) {
-    const int v = base + lane;
-    float x[N];
-    int nvalid = 0;
-    if (v < ve) {
-      load(v, x);
-      nvalid = min(N, n - v * N);
-    } else {
+  for (int base = vb; base < ve; base += 32 * U) {
+    float x[U][N];
+    int nvalid[U];
 #pragma unroll
-      for (int j = 0; j < N; ++j) x[j] = -INFINITY;
+    for (int u = 0; u < U; ++u) {
+      const int v = base + 32 * u + lane;
+      nvalid[u] = 0;
+      if (v < ve) {
+        load(v, x[u]);
+        nvalid[u] = min(N, n - v * N);
+      } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) x[u][j] = -INFINITY;
+      }
     }
-    f(x, v * N, nvalid);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + 32 * u < ve) f(x[u], (base + 32 * u + lane) * N, nvalid[u]);
   }
 }
 
@@ -323,10 +334,10 @@ __device__ __forceinline__ void for_warp_segment(int n, int warp, int lane, Load
 // per-iteration warp total (float, xor tree) of each lane's per-vector sum
 // (float, element order).  warp_ordered_draw repeats exactly this arithmetic,
 // so a total and a later scan of the same weights agree bit for bit.
-template <int N, typename Load, typename WL>
+template <int N, int U = 1, typename Load, typename WL>
 __device__ double warp_ordered_total(int n, int warp, int lane, Load load, WL wl) {
   double running = 0.0;
-  for_warp_segment<N>(n, warp, lane, load, [&](float (&x)[N], int e0, int nvalid) {
+  for_warp_segment<N, U>(n, warp, lane, load, [&](float (&x)[N], int e0, int nvalid) {
     wl(x, e0, nvalid);
     float s = 0.0f;
 #pragma unroll
@@ -340,13 +351,13 @@ __device__ double warp_ordered_total(int n, int warp, int lane, Load load, WL wl
 // find the smallest element index e with target < base + cumsum(e).  With
 // `overflow` (target beyond every total) the last element with positive weight
 // is returned instead.  Returns the segment-local element index on all lanes.
-template <int N, typename Load, typename WL>
+template <int N, int U = 1, typename Load, typename WL>
 __device__ int warp_ordered_draw(int n, int warp, int lane, Load load, WL wl, double target, double base,
                                  bool overflow) {
   double running = base;
   int found = -1, last_pos = -1;
   bool done = false;
-  for_warp_segment<N>(n, warp, lane, load, [&](float (&x)[N], int e0, int nvalid) {
+  for_warp_segment<N, U>(n, warp, lane, load, [&](float (&x)[N], int e0, int nvalid) {
     if (done) return;  // warp-uniform
     wl(x, e0, nvalid);
     float s = 0.0f;
@@ -392,9 +403,13 @@ __device__ int warp_ordered_draw(int n, int warp, int lane, Load load, WL wl, do
 }
 
 // ---------------------------------------------------------------------------
-// cluster exchange.  Thread 0 fills sm.slot[C.ph] first; exchange() is a cluster
-// barrier (release/acquire) after which every CTA may read all ranks' slots of
-// that phase until its next exchange().  Every thread tracks the phase itself.
+// cluster exchange.  Thread 0 (or one lane) fills sm.slot[C.ph] first;
+// exchange() is a cluster barrier (release/acquire), after which all threads copy
+// every rank's slot of that phase into the local mirror at once -- one round of
+// distributed-shared-memory loads instead of a serial chain -- and return it.
+// Slots alternate between two buffers, so a rank may overwrite its slot for the
+// next exchange while others still copy the previous one.  The mirror stays
+// valid until the next exchange().  Every thread tracks the phase itself.
 
 struct Cluster {
   cg::cluster_group cl;
@@ -404,12 +419,18 @@ struct Cluster {
     rank = static_cast<int>(cl.block_rank());
   }
   __device__ Slot& mine(Scratch& sm) { return sm.slot[ph]; }
-  __device__ const Slot* remote(Scratch& sm, int phase, int r) { return cl.map_shared_rank(&sm.slot[phase], r); }
-  __device__ int exchange() {
+  __device__ const Slot* exchange(Scratch& sm) {
     const int p = ph;
     cl.sync();
     ph ^= 1;
-    return p;
+    constexpr int W = static_cast<int>(sizeof(Slot) / sizeof(uint32_t));
+    for (int i = threadIdx.x; i < cs * W; i += kThreads) {
+      const int r = i / W, o = i - r * W;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(cl.map_shared_rank(&sm.slot[p], r));
+      reinterpret_cast<uint32_t*>(&sm.mirror[r])[o] = src[o];
+    }
+    __syncthreads();
+    return sm.mirror;
   }
 };
 
@@ -535,12 +556,12 @@ __device__ void load_and_scan(const KArgs& a, const RowCtx<E>& rc, E* sl, Scratc
     s.i[0] = bi;
     s.i[1] = fl;
   }
-  const int ph = C.exchange();
+  const Slot* mir = C.exchange(sm);
   if (tid == 0) {
     float bv = -INFINITY;
     int bi = INT_MAX, fl = 0;
     for (int r = 0; r < C.cs; ++r) {
-      const Slot* s = C.remote(sm, ph, r);
+      const Slot* s = (&mir[r]);
       const float v = static_cast<float>(s->d[0]);
       const int i = s->i[0];
       if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
@@ -555,10 +576,10 @@ __device__ void load_and_scan(const KArgs& a, const RowCtx<E>& rc, E* sl, Scratc
 }
 
 // ---- cluster-wide ordered total of weights over the resident row -------------
-// Leaves per-(rank, warp) totals in every CTA's slot d[1 + w] of the returned
-// phase, for a following cluster_ordered_draw with the same weights.
+// Leaves per-(rank, warp) totals in the mirror (d[1 + w] of each rank), for a
+// following cluster_ordered_draw with the same weights and no exchange between.
 template <typename E, typename WF>
-__device__ double cluster_weight_total(const RowCtx<E>& rc, Scratch& sm, Cluster& C, WF wf, int* ph_out) {
+__device__ double cluster_weight_total(const RowCtx<E>& rc, Scratch& sm, Cluster& C, WF wf) {
   constexpr int N = Fmt<E>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   auto wl = [&](float (&x)[N], int e0, int nvalid) {
@@ -577,37 +598,37 @@ __device__ double cluster_weight_total(const RowCtx<E>& rc, Scratch& sm, Cluster
     }
     s.d[0] = tot;
   }
-  const int ph = C.exchange();
+  const Slot* mir = C.exchange(sm);
   if (threadIdx.x == 0) {
     double z = 0.0;
-    for (int r = 0; r < C.cs; ++r) z += C.remote(sm, ph, r)->d[0];
+    for (int r = 0; r < C.cs; ++r) z += (&mir[r])->d[0];
     sm.bd[0] = z;
   }
   __syncthreads();
   const double z = sm.bd[0];
   __syncthreads();
-  *ph_out = ph;
   return z;
 }
 
 // Ordered draw over the cluster-resident row with the weights of the preceding
-// cluster_weight_total (phase ph).  The finding warp writes the token through
+// cluster_weight_total (its totals still in the mirror).  The finding warp writes the token through
 // `emit(token)`.
 template <typename E, typename WF, typename Emit>
-__device__ void cluster_ordered_draw(const RowCtx<E>& rc, Scratch& sm, Cluster& C, int ph, double u, WF wf,
+__device__ void cluster_ordered_draw(const RowCtx<E>& rc, Scratch& sm, Cluster& C, double u, WF wf,
                                      Emit emit) {
+  const Slot* mir = sm.mirror;
   constexpr int N = Fmt<E>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     double total = 0.0;
     for (int r = 0; r < C.cs; ++r)
-      for (int w = 0; w < kWarps; ++w) total += C.remote(sm, ph, r)->d[1 + w];
+      for (int w = 0; w < kWarps; ++w) total += (&mir[r])->d[1 + w];
     const double target = u * total;
     int fr = -1, fw = -1, lr = 0, lw = 0;
     double base = 0.0, cum = 0.0;
     for (int r = 0; r < C.cs && fr < 0; ++r)
       for (int w = 0; w < kWarps; ++w) {
-        const double t = C.remote(sm, ph, r)->d[1 + w];
+        const double t = (&mir[r])->d[1 + w];
         if (t > 0.0) { lr = r; lw = w; }
         if (target < cum + t) { fr = r; fw = w; base = cum; break; }
         cum += t;
@@ -678,11 +699,11 @@ __device__ void probe_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, const f
       s.d[p] = ms;
     }
   }
-  const int ph = C.exchange();
+  const Slot* mir = C.exchange(sm);
   if (threadIdx.x == 0) {
     for (int p = 0; p < np; ++p) { sm.bi[p] = 0; sm.bd[p] = 0.0; }
     for (int r = 0; r < C.cs; ++r) {
-      const Slot* s = C.remote(sm, ph, r);
+      const Slot* s = (&mir[r]);
       for (int p = 0; p < np; ++p) { sm.bi[p] += s->i[p]; sm.bd[p] += s->d[p]; }
     }
   }
@@ -880,23 +901,19 @@ __device__ int gather_candidates(const RowCtx<E>& rc, Scratch& sm, Cluster& C, f
     if (pos < kCap) { sm.cand_idx[pos] = x; sm.cand_val[pos] = l; }
   });
   if (threadIdx.x == 0) C.mine(sm).i[0] = n;
-  const int ph = C.exchange();
-  if (threadIdx.x == 0) {
-    int total = 0;
-    for (int r = 0; r < C.cs; ++r) total += C.remote(sm, ph, r)->i[0];
-    sm.bi[0] = total;
-  }
-  __syncthreads();
-  const int total = sm.bi[0];
+  const Slot* mir = C.exchange(sm);
+  int off[kMaxCluster + 1];
+  off[0] = 0;
+  for (int r = 0; r < C.cs; ++r) off[r + 1] = off[r] + mir[r].i[0];
+  const int total = off[C.cs];
   if (C.rank == 0) {
-    int off = n;
-    for (int r = 1; r < C.cs; ++r) {
-      const int cr = C.remote(sm, ph, r)->i[0];
-      const int32_t* ri = C.cl.map_shared_rank(sm.cand_idx, r);
-      const float* rv = C.cl.map_shared_rank(sm.cand_val, r);
-      for (int i = threadIdx.x; i < cr; i += kThreads)
-        if (off + i < kCap) { sm.cand_idx[off + i] = ri[i]; sm.cand_val[off + i] = rv[i]; }
-      off += cr;
+    // one flat round of remote loads: position j comes from the rank whose range holds it
+    for (int j = n + threadIdx.x; j < min(total, kCap); j += kThreads) {
+      int r = 1;
+      while (r + 1 < C.cs && j >= off[r + 1]) ++r;
+      const int i = j - off[r];
+      sm.cand_idx[j] = C.cl.map_shared_rank(sm.cand_idx, r)[i];
+      sm.cand_val[j] = C.cl.map_shared_rank(sm.cand_val, r)[i];
     }
   }
   __syncthreads();
@@ -966,12 +983,12 @@ __device__ int tie_locate(const RowCtx<E>& rc, Scratch& sm, Cluster& C, float ti
     Slot& s = C.mine(sm);
     for (int w = 0; w < kWarps; ++w) s.i[1 + w] = sm.wi[w];
   }
-  int ph = C.exchange();
+  const Slot* mir = C.exchange(sm);
   if (threadIdx.x == 0) {
     int acc = 0, fr = -1, fw = -1, kth = 0;
     for (int r = 0; r < C.cs && fr < 0; ++r)
       for (int w = 0; w < kWarps; ++w) {
-        const int cw = C.remote(sm, ph, r)->i[1 + w];
+        const int cw = (&mir[r])->i[1 + w];
         if (acc + cw >= c) { fr = r; fw = w; kth = c - acc; break; }
         acc += cw;
       }
@@ -1003,8 +1020,8 @@ __device__ int tie_locate(const RowCtx<E>& rc, Scratch& sm, Cluster& C, float ti
     found = warp_max_i(found);
     if (lane == 0) C.mine(sm).i[0] = found;
   }
-  ph = C.exchange();
-  if (threadIdx.x == 0) sm.bi[3] = (fr >= 0) ? C.remote(sm, ph, fr)->i[0] : INT_MAX;
+  mir = C.exchange(sm);
+  if (threadIdx.x == 0) sm.bi[3] = (fr >= 0) ? mir[fr].i[0] : INT_MAX;
   __syncthreads();
   const int idx = sm.bi[3];
   __syncthreads();
@@ -1037,12 +1054,12 @@ __device__ void kept_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, Cut cut,
     s.d[0] = t;
     s.i[0] = ct;
   }
-  const int ph = C.exchange();
+  const Slot* mir = C.exchange(sm);
   if (threadIdx.x == 0) {
     double z = 0.0;
     int total = 0, off = 0;
     for (int r = 0; r < C.cs; ++r) {
-      const Slot* s = C.remote(sm, ph, r);
+      const Slot* s = (&mir[r]);
       z += s->d[0];
       if (r < C.rank) off += s->i[0];
       total += s->i[0];
@@ -1136,7 +1153,7 @@ __device__ int global_rows_draw(const KArgs& a, const E* gt, const E* gd, float 
     for (int j = 0; j < N; ++j)
       if (j >= nvalid) x[j] = 0.0f;
   };
-  const double wt = warp_ordered_total<N>(V, warp, lane, load, wl);
+  const double wt = warp_ordered_total<N, 4>(V, warp, lane, load, wl);
   if (lane == 0) sm.wtot[warp] = wt;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -1164,7 +1181,7 @@ __device__ int global_rows_draw(const KArgs& a, const E* gt, const E* gd, float 
   const bool overflow = sm.bi[1] != 0;
   const double target = sm.bd[0], base = sm.bd[1];
   if (fw >= 0 && warp == fw) {
-    const int e = warp_ordered_draw<N>(V, warp, lane, load, wl, target, base, overflow);
+    const int e = warp_ordered_draw<N, 4>(V, warp, lane, load, wl, target, base, overflow);
     if (lane == 0) sm.bi[2] = e;
   }
   __syncthreads();
@@ -1182,27 +1199,27 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
   const spec_row_stat* recs = a.rows + static_cast<int64_t>(b) * R;
   int32_t* out = a.out_tokens + static_cast<int64_t>(b) * (K + 1);
   const int tid = threadIdx.x;
-  if (tid == 0) {
-    int fl = 0;
-    for (int r = 0; r < R; ++r) fl |= __ldcg(&recs[r].flags);
-    int n = K;
-    if (!fl) {
-      for (int t = 0; t < K; ++t) {
-        const int d = a.tokens[static_cast<int64_t>(b) * K + t];
-        bool acc;
-        if (a.greedy) {
-          acc = (d == __ldcg(&recs[t].argmax));
-        } else {
-          // keep d_t with probability min(1, tgt/drf):  u * drf < tgt
-          const double pt = __ldcg(&recs[t].p_tok);
-          const double pd = __ldcg(&recs[K + 1 + t].p_tok);
-          acc = a.u[static_cast<int64_t>(b) * (K + 1) + t] * pd < pt;
-        }
-        if (!acc) { n = t; break; }
+  // all row records in parallel: flags, then the first rejection (one test per thread)
+  if (tid == 0) { sm.bi[12] = 0; sm.bi[13] = K; }
+  __syncthreads();
+  int myfl = 0;
+  for (int r = tid; r < R; r += kThreads) myfl |= __ldcg(&recs[r].flags);
+  if (myfl) atomicOr(&sm.bi[12], myfl);
+  __syncthreads();
+  if (sm.bi[12] == 0) {
+    for (int t = tid; t < K; t += kThreads) {
+      const int d = a.tokens[static_cast<int64_t>(b) * K + t];
+      bool acc;
+      if (a.greedy) {
+        acc = (d == __ldcg(&recs[t].argmax));
+      } else {
+        // keep d_t with probability min(1, tgt/drf):  u * drf < tgt
+        const double pt = __ldcg(&recs[t].p_tok);
+        const double pd = __ldcg(&recs[K + 1 + t].p_tok);
+        acc = a.u[static_cast<int64_t>(b) * (K + 1) + t] * pd < pt;
       }
+      if (!acc) atomicMin(&sm.bi[13], t);  // the first rejection wins
     }
-    sm.bi[12] = fl;
-    sm.bi[13] = n;
   }
   __syncthreads();
   const int fl = sm.bi[12], n = sm.bi[13];
@@ -1233,15 +1250,20 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
       // kept sets stored: residual over the target's kept list (index order)
       const int32_t* ti = a.list_idx + job_t * kCap;
       const float* tw = a.list_w + job_t * kCap;
-      const int32_t* di = a.list_idx + job_d * kCap;
-      const float* dw = a.list_w + job_d * kCap;
+      // the draft's kept list goes to shared memory (the candidate arrays are free now)
+      if (resid) {
+        const int32_t* di = a.list_idx + job_d * kCap;
+        const float* dw = a.list_w + job_d * kCap;
+        for (int i = tid; i < ld; i += kThreads) { sm.cand_idx[i] = __ldcg(&di[i]); sm.cand_val[i] = __ldcg(&dw[i]); }
+        __syncthreads();
+      }
       auto drf_w = [&](int x) -> double {
         int lo = 0, hi = ld;
         while (lo < hi) {
           const int mid = (lo + hi) >> 1;
-          if (__ldcg(&di[mid]) < x) lo = mid + 1; else hi = mid;
+          if (sm.cand_idx[mid] < x) lo = mid + 1; else hi = mid;
         }
-        return (lo < ld && __ldcg(&di[lo]) == x) ? static_cast<double>(__ldcg(&dw[lo])) : 0.0;
+        return (lo < ld && sm.cand_idx[lo] == x) ? static_cast<double>(sm.cand_val[lo]) : 0.0;
       };
       int pos = -1;
       if (resid)
@@ -1311,15 +1333,14 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
   double zf = 1.0;
   int list_len = -1;
   bool rank0_list = false;  // kept list sits in rank 0's candidate arrays
-  int draw_ph = -1;         // phase of unfiltered weight totals (sample draw)
 
   if (!bad && !a.greedy) {
     auto wall = [&](float l, int) { return wexp(l, rc.m, rc.c); };
     if (!use_k && !use_p) {
-      zf = cluster_weight_total<E>(rc, sm, C, wall, &draw_ph);
+      zf = cluster_weight_total<E>(rc, sm, C, wall);
     } else {
       double zk = 0.0;
-      if (!use_k) zk = cluster_weight_total<E>(rc, sm, C, wall, &draw_ph);
+      if (!use_k) zk = cluster_weight_total<E>(rc, sm, C, wall);
       bool restricted = false;
       Cut kcut = cut_all();
       bool final_tie = false;
@@ -1402,7 +1423,7 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
     } else if (rank0_list || list_len >= 0) {
       // kept list stored: draw over it (rank 0)
       if (!rank0_list) { __threadfence(); }
-      C.exchange();  // lists written by every CTA are visible after the barrier
+      C.cl.sync();  // lists written by every CTA are visible after the barrier
       if (C.rank == 0) {
         const int pos = list_ordered_draw(list_len, u, sm, [&](int i) { return static_cast<double>(__ldcg(&lw[i])); });
         if (tid == 0) {
@@ -1414,11 +1435,9 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
     } else {
       // no stored list: ordered draw over the resident row
       auto wk = [&](float l, int x) { return cut.keep(l, x) ? wexp(l, rc.m, rc.c) : 0.0f; };
-      if (draw_ph < 0 || use_k || use_p) {
-        double z2 = cluster_weight_total<E>(rc, sm, C, wk, &draw_ph);
-        (void)z2;
-      }
-      cluster_ordered_draw<E>(rc, sm, C, draw_ph, u, wk, [&](int tok) {
+      // unfiltered rows: the totals of the normaliser pass are still in the mirror
+      if (use_k || use_p) (void)cluster_weight_total<E>(rc, sm, C, wk);
+      cluster_ordered_draw<E>(rc, sm, C, u, wk, [&](int tok) {
         *outp = tok;
         rec->token = tok;
       });
