@@ -66,7 +66,8 @@ typedef enum {
   SPEC_ERR_NONFINITE = 3,    /* device: NaN or +inf logit, or no finite logit, in a row read */
   SPEC_ERR_TOKEN_RANGE = 4,  /* device: a draft token outside [0, V) */
   SPEC_ERR_TIMEOUT = 5,      /* device: a bounded wait on an asynchronous copy ran out */
-  SPEC_ERR_UNSUPPORTED = 6   /* host: V too large for one row per thread-block cluster */
+  SPEC_ERR_UNSUPPORTED = 6,  /* host: V too large for one row per thread-block cluster */
+  SPEC_ERR_SCRATCH_LIMIT = 7 /* host: spec_verify_noalloc asked for more than its fixed scratch */
 } spec_status;
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
@@ -155,6 +156,41 @@ spec_status spec_sample_draft(const void* draft_logits, const double* uniforms,
  * Returns SPEC_ERR_INVALID_ARG if max_rows is smaller than the row count. */
 spec_status spec_read_row_stats(const spec_params* params, int32_t is_verify,
                                 spec_row_stat* host_out, int64_t max_rows);
+
+/* Scratch size of spec_verify_noalloc: 8 MiB, enough for about 2000 rows
+ * (B * (2K+1) sampling, B * (K+1) greedy). */
+#define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* spec_verify for callers that cannot allocate device memory.  Not a step of
+ * the method: the pages have no counterpart; it only changes where the scratch
+ * lives.
+ *
+ * Who needs it: a plugin inside a serving framework that has already reserved
+ * the GPU's memory for its own pool (weights, KV cache) and hands the plugin
+ * only the tensors it works on -- a cudaMalloc from the plugin would fail or
+ * fragment that pool, and a plain C ABI gives it no handle to the framework's
+ * allocator; and decode loops that must not allocate between tokens, because
+ * cudaMalloc can synchronise the device.
+ *
+ * Same arguments and results as spec_verify; params->workspace and
+ * params->workspace_bytes are ignored.  The scratch is one array of
+ * SPEC_NOALLOC_SCRATCH_BYTES in device global memory, defined in the library,
+ * which every GPU that loads the library keeps until the process exits.  The
+ * first call on a device (made with that device current) looks up the array's
+ * device address once; make that first call before any stream capture.
+ *
+ *   - Every call uses the same array, which keeps the last call's contents.
+ *     Nothing in it has to start at zero (the per-sequence counters carry a
+ *     per-call tag), so no clearing is needed between calls.
+ *   - Calls whose work overlaps on the GPU (other streams, other threads)
+ *     share the array and race: serialise them.
+ *   - Returns SPEC_ERR_SCRATCH_LIMIT, with nothing launched, when
+ *     spec_verify_workspace_size(params) exceeds SPEC_NOALLOC_SCRATCH_BYTES.
+ *   - Never calls cudaMalloc, cudaFree or any allocating routine. */
+spec_status spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                                const int32_t* draft_tokens, const double* uniforms,
+                                const spec_params* params, int32_t* out_tokens,
+                                int32_t* out_num_accepted);
 
 /* Static description of a status code. */
 const char* spec_status_string(spec_status status);

@@ -19,10 +19,12 @@ from . import _build
 SPEC_OK = 0
 SPEC_F32, SPEC_BF16 = 0, 1
 STATUS_NAMES = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_CUDA", 3: "SPEC_ERR_NONFINITE",
-                4: "SPEC_ERR_TOKEN_RANGE", 5: "SPEC_ERR_TIMEOUT", 6: "SPEC_ERR_UNSUPPORTED"}
+                4: "SPEC_ERR_TOKEN_RANGE", 5: "SPEC_ERR_TIMEOUT", 6: "SPEC_ERR_UNSUPPORTED",
+                7: "SPEC_ERR_SCRATCH_LIMIT"}
+SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
 EXPORTED = ("spec_verify", "spec_sample_draft", "spec_verify_workspace_size",
             "spec_sample_draft_workspace_size", "spec_read_row_stats", "spec_status_string",
-            "spec_launch_count")
+            "spec_launch_count", "spec_verify_noalloc")
 
 
 class SpecParams(ctypes.Structure):
@@ -81,6 +83,8 @@ def lib() -> ctypes.CDLL:
             L.spec_read_row_stats.restype = ctypes.c_int
             L.spec_status_string.argtypes = [ctypes.c_int]
             L.spec_status_string.restype = ctypes.c_char_p
+            L.spec_verify_noalloc.argtypes = [P, P, P, P, PP, P, P]
+            L.spec_verify_noalloc.restype = ctypes.c_int
             L.spec_launch_count.argtypes = []
             L.spec_launch_count.restype = ctypes.c_uint64
             _lib = L
@@ -227,3 +231,26 @@ def spec_read_row_stats(B, K, V, dtype, is_verify, ws, *, greedy=False, temperat
     if code != SPEC_OK:
         raise SpecError(code, "spec_read_row_stats")
     return [{f: getattr(arr[i], f) for f, _ in SpecRowStat._fields_ if f != "pad_"} for i in range(n)]
+
+
+def spec_verify_noalloc(target, draft, draft_tokens, uniforms, *, temperature=1.0, top_k=0, top_p=1.0,
+                        greedy=False, out_tokens=None, out_num_accepted=None, status=None, stream=None):
+    """spec_verify with the library's fixed scratch array instead of a workspace, for
+    callers that may not allocate device memory (see include/spec_verify.h).  Same
+    arguments and results as spec_verify."""
+    _check_cuda(target, draft, draft_tokens, uniforms)
+    K, B, V = draft_tokens.shape[1], draft_tokens.shape[0], target.shape[-1]
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    dstr = (draft.stride(0), draft.stride(1)) if draft is not None else (0, 0)
+    p = make_params(B, K, V, _dtype_code(target), (target.stride(0), target.stride(1)), dstr,
+                    temperature, top_k, top_p, greedy, _stream_handle(stream), status)
+    code = lib().spec_verify_noalloc(_ptr(target), _ptr(draft), _ptr(draft_tokens.contiguous()),
+                                     _ptr(None if uniforms is None else uniforms.contiguous()),
+                                     ctypes.byref(p), _ptr(out_tokens), _ptr(out_num_accepted))
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_verify_noalloc")
+    return out_tokens, out_num_accepted

@@ -1768,6 +1768,7 @@ const char* spec_status_string(spec_status status) {
     case SPEC_ERR_TOKEN_RANGE: return "draft token outside [0, V)";
     case SPEC_ERR_TIMEOUT: return "bounded wait on an asynchronous copy ran out";
     case SPEC_ERR_UNSUPPORTED: return "vocabulary too large for one row per thread-block cluster";
+    case SPEC_ERR_SCRATCH_LIMIT: return "request needs more scratch than spec_verify_noalloc's fixed array";
   }
   return "unknown status";
 }
@@ -1775,3 +1776,51 @@ const char* spec_status_string(spec_status status) {
 uint64_t spec_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"
+
+// ===========================================================================
+// spec_verify without caller memory: the scratch is a fixed device array.
+
+namespace {
+
+constexpr size_t kNoAllocBytes = SPEC_NOALLOC_SCRATCH_BYTES;
+// Lives in every GPU that loads the library, until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// The array's name is only a host-side stand-in: its device address is looked
+// up once per device, with that device current, and reused.
+spec_status noalloc_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SPEC_ERR_CUDA;
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" spec_status spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                                           const int32_t* draft_tokens, const double* uniforms,
+                                           const spec_params* params, int32_t* out_tokens,
+                                           int32_t* out_num_accepted) {
+  if (!params) return SPEC_ERR_INVALID_ARG;
+  spec_params p = *params;
+  p.workspace = nullptr;
+  p.workspace_bytes = 0;
+  const size_t need = spec_verify_workspace_size(&p);
+  if (need == 0) return SPEC_ERR_INVALID_ARG;
+  if (need > kNoAllocBytes) return SPEC_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  const spec_status s = noalloc_address(&scratch);
+  if (s != SPEC_OK) return s;
+  p.workspace = scratch;
+  p.workspace_bytes = kNoAllocBytes;
+  return spec_verify(target_logits, draft_logits, draft_tokens, uniforms, &p, out_tokens, out_num_accepted);
+}
