@@ -27,6 +27,7 @@
 //     last cluster of a sequence to finish (atomic ticket, no spinning) runs
 //     the accept tests and the one final draw for that sequence.
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -46,6 +47,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 512;       // on-chip sort capacity == stored kept-list capacity
+constexpr int kWarpCap = kCap / 8;  // first-pass candidate list per warp (8 warps)
 constexpr int kProbes = 8;      // thresholds evaluated per probe pass
 constexpr int kStages = 4;      // bulk-copy stages per slice
 constexpr int kMaxCluster = 8;  // portable cluster size
@@ -79,14 +81,16 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// The thread sleeps in hardware until the phase completes or ~1 ms passes, so
+// waiting warps do not spin and take no issue slots from the working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
@@ -100,9 +104,9 @@ __device__ __forceinline__ uint64_t global_ns() {
 __device__ bool mbar_wait_bounded(uint64_t* bar) {
   if (mbar_try_wait(bar, 0)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t it = 0; it < (1u << 24); ++it) {
+  for (uint32_t it = 0; it < 100000u; ++it) {
     if (mbar_try_wait(bar, 0)) return true;
-    if ((it & 63u) == 63u && global_ns() - t0 > 2000000000ull) break;
+    if (global_ns() - t0 > 2000000000ull) break;
   }
   return false;
 }
@@ -127,6 +131,16 @@ struct Fmt<float> {
     x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
   }
   __device__ static float at(const float* s, int64_t e) { return s[e]; }
+  // max of vector v (NaN-propagating) and whether it holds a NaN
+  __device__ static float vec_max(const float* s, int v, bool& nan) {
+    const float4 q = reinterpret_cast<const float4*>(s)[v];
+    float a, b, r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(a) : "f"(q.x), "f"(q.y));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(b) : "f"(q.z), "f"(q.w));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    nan = r != r;
+    return r;
+  }
   __device__ static float at_global(const float* g, int64_t e) { return __ldg(g + e); }
   // order-preserving key over the data's own grid (32-bit for fp32)
   __device__ static uint32_t key(float f) {
@@ -157,6 +171,21 @@ struct Fmt<uint16_t> {  // bf16 carried as raw bits
     unpack(__ldg(reinterpret_cast<const uint4*>(g) + v), x);
   }
   __device__ static float at(const uint16_t* s, int64_t e) { return bf16_bits_to_float(s[e]); }
+  // max of vector v (NaN-propagating, on packed bf16 pairs) and whether it holds a NaN
+  __device__ static float vec_max(const uint16_t* s, int v, bool& nan) {
+    const uint4 q = reinterpret_cast<const uint4*>(s)[v];
+    __nv_bfloat162 a, b, c, d;
+    memcpy(&a, &q.x, 4);
+    memcpy(&b, &q.y, 4);
+    memcpy(&c, &q.z, 4);
+    memcpy(&d, &q.w, 4);
+    const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+    uint32_t mw;
+    memcpy(&mw, &m, 4);
+    const float lo = __uint_as_float(mw << 16), hi = __uint_as_float(mw & 0xffff0000u);
+    nan = (lo != lo) || (hi != hi);
+    return fmaxf(lo, hi);
+  }
   __device__ static float at_global(const uint16_t* g, int64_t e) {
     return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(g) + e));
   }
@@ -186,6 +215,46 @@ __device__ __forceinline__ float okey32_val(uint32_t k) {
 __device__ __forceinline__ float wexp(float l, float m, float c) { return exp2f((l - m) * c); }
 
 // ---------------------------------------------------------------------------
+// float-float ("double-single") sums.  GB300 runs FP64 at a small fraction of
+// its FP32 rate, so running totals, prefix sums and cluster reductions keep a
+// (hi, lo) pair of floats: Knuth's TwoSum for additions and an FMA-based
+// TwoProduct for scaling give ~48-bit significands on the FP32 pipes.  Doubles
+// appear only in single-thread spots (the accept test, record fields).
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff(float x) { return FF{x, 0.0f}; }
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  float e = (a.hi - (s - bb)) + (b.hi - bb);  // exact rounding error of s
+  e += a.lo + b.lo;
+  const float hi = s + e;
+  return FF{hi, e - (hi - s)};
+}
+__device__ __forceinline__ FF ff_add(FF a, float b) { return ff_add(a, ff(b)); }
+__device__ __forceinline__ FF ff_sub(FF a, FF b) { return ff_add(a, FF{-b.hi, -b.lo}); }
+__device__ __forceinline__ FF ff_mul(FF a, float b) {
+  const float p = a.hi * b;
+  float e = fmaf(a.hi, b, -p);  // exact rounding error of p
+  e = fmaf(a.lo, b, e);
+  const float hi = p + e;
+  return FF{hi, e - (hi - p)};
+}
+__device__ __forceinline__ bool ff_lt(FF a, FF b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+__device__ __forceinline__ double ff_to_d(FF a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
+__device__ __forceinline__ FF ff_from_d(double d) {
+  const float hi = static_cast<float>(d);
+  return FF{hi, static_cast<float>(d - static_cast<double>(hi))};
+}
+__device__ __forceinline__ FF shfl_up_ff(FF v, int o) {
+  return FF{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ FF shfl_ff(FF v, int src) {
+  return FF{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+// ---------------------------------------------------------------------------
 // kernel arguments and shared scratch
 
 struct KArgs {
@@ -208,7 +277,7 @@ struct KArgs {
 };
 
 struct Slot {  // per-CTA values published to the cluster
-  double d[kProbes + kWarps + 4];
+  FF d[kProbes + kWarps + 4];
   int32_t i[kProbes + kWarps + 4];
 };
 
@@ -220,14 +289,14 @@ struct alignas(128) Scratch {
   float wf[kWarps];
   int32_t wi[kWarps];
   int32_t wi2[kWarps];
-  double wd[kWarps];
+  FF wd[kWarps];
   int32_t pcnt[kProbes][kWarps];
   float pmass[kProbes][kWarps];
-  double wtot[kWarps];
+  FF wtot[kWarps];
   // values broadcast to the whole CTA by thread 0
   float m;
   int32_t argmax, bad, abort_;
-  double bd[kProbes + 4];
+  FF bd[kProbes + 4];
   int32_t bi[kProbes + 8];
   // candidates: this CTA's, and on rank 0 the cluster's gathered list
   int32_t cand_idx[kCap];
@@ -238,9 +307,9 @@ struct alignas(128) Scratch {
 // slice is no longer read once the candidates are gathered.
 struct SortBuf {
   unsigned long long* skey;  // [kCap]
-  double* scan;              // [kCap]
+  FF* scan;                  // [kCap]
 };
-constexpr size_t kSortBufBytes = kCap * (sizeof(unsigned long long) + sizeof(double));
+constexpr size_t kSortBufBytes = kCap * (sizeof(unsigned long long) + sizeof(FF));
 // scratch + a 64 KB slice must leave room for three CTAs in an SM's 228 KB
 static_assert(sizeof(Scratch) <= 8192, "shared scratch grew past its budget");
 static_assert(sizeof(Slot) % sizeof(uint32_t) == 0, "slots are copied as 32-bit words");
@@ -271,26 +340,45 @@ __device__ __forceinline__ int warp_incl_scan_i(int v, int lane) {
   }
   return v;
 }
-__device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
+__device__ __forceinline__ FF warp_incl_scan_ff(FF v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(FULL, v, o);
-    if (lane >= o) v += t;
+    const FF t = shfl_up_ff(v, o);
+    if (lane >= o) v = ff_add(t, v);
   }
   return v;
 }
 
-// Exclusive block scan of one double per thread (fixed order); *total gets the
-// block total.  Uses sm.wd.
-__device__ double block_excl_scan_d(double v, double* total, Scratch& sm) {
+// Exclusive block scan of one float-float per thread (fixed order); *total gets
+// the block total.  Uses sm.wd.
+__device__ FF block_excl_scan_ff(FF v, FF* total, Scratch& sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const double incl = warp_incl_scan_d(v, lane);
+  const FF incl = warp_incl_scan_ff(v, lane);
+  FF excl = shfl_up_ff(incl, 1);
+  if (lane == 0) excl = ff(0.0f);
   if (lane == 31) sm.wd[warp] = incl;
   __syncthreads();
-  double before = 0.0, tot = 0.0;
+  FF before = ff(0.0f), tot = ff(0.0f);
   for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) before += sm.wd[w];
-    tot += sm.wd[w];
+    if (w == warp) before = tot;
+    tot = ff_add(tot, sm.wd[w]);
+  }
+  __syncthreads();
+  *total = tot;
+  return ff_add(before, excl);
+}
+
+// Exclusive block scan of one int per thread; *total gets the block total.
+// Uses sm.wi.
+__device__ int block_excl_scan_i(int v, int* total, Scratch& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int incl = warp_incl_scan_i(v, lane);
+  if (lane == 31) sm.wi[warp] = incl;
+  __syncthreads();
+  int before = 0, tot = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) before += sm.wi[w];
+    tot += sm.wi[w];
   }
   __syncthreads();
   *total = tot;
@@ -330,19 +418,19 @@ __device__ __forceinline__ void for_warp_segment(int n, int warp, int lane, Load
 }
 
 // Ordered weights: wl(v, x, nvalid) turns vector v's values x into weights in
-// place (entries j >= nvalid must become 0).  Per warp, running (double) +=
+// place (entries j >= nvalid must become 0).  Per warp, running (float-float) +=
 // per-iteration warp total (float, xor tree) of each lane's per-vector sum
 // (float, element order).  warp_ordered_draw repeats exactly this arithmetic,
 // so a total and a later scan of the same weights agree bit for bit.
 template <int N, int U = 1, typename Load, typename WL>
-__device__ double warp_ordered_total(int n, int warp, int lane, Load load, WL wl) {
-  double running = 0.0;
+__device__ FF warp_ordered_total(int n, int warp, int lane, Load load, WL wl) {
+  FF running = ff(0.0f);
   for_warp_segment<N, U>(n, warp, lane, load, [&](float (&x)[N], int e0, int nvalid) {
     wl(x, e0, nvalid);
     float s = 0.0f;
 #pragma unroll
     for (int j = 0; j < N; ++j) s += x[j];
-    running += static_cast<double>(warp_sum_f(s));
+    running = ff_add(running, warp_sum_f(s));
   });
   return running;
 }
@@ -352,9 +440,9 @@ __device__ double warp_ordered_total(int n, int warp, int lane, Load load, WL wl
 // `overflow` (target beyond every total) the last element with positive weight
 // is returned instead.  Returns the segment-local element index on all lanes.
 template <int N, int U = 1, typename Load, typename WL>
-__device__ int warp_ordered_draw(int n, int warp, int lane, Load load, WL wl, double target, double base,
+__device__ int warp_ordered_draw(int n, int warp, int lane, Load load, WL wl, FF target, FF base,
                                  bool overflow) {
-  double running = base;
+  FF running = base;
   int found = -1, last_pos = -1;
   bool done = false;
   for_warp_segment<N, U>(n, warp, lane, load, [&](float (&x)[N], int e0, int nvalid) {
@@ -366,21 +454,21 @@ __device__ int warp_ordered_draw(int n, int warp, int lane, Load load, WL wl, do
       s += x[j];
       if (x[j] > 0.0f) last_pos = max(last_pos, e0 + j);
     }
-    const double it = static_cast<double>(warp_sum_f(s));
-    if (!overflow && target < running + it) {
-      const double incl = warp_incl_scan_d(static_cast<double>(s), lane);
-      const unsigned hit = __ballot_sync(FULL, target < running + incl);
+    const float it = warp_sum_f(s);
+    if (!overflow && ff_lt(target, ff_add(running, it))) {
+      const FF incl = warp_incl_scan_ff(ff(s), lane);
+      const unsigned hit = __ballot_sync(FULL, ff_lt(target, ff_add(running, incl)));
       int tok = -1;
       if (hit) {
         const int hl = __ffs(hit) - 1;
         if (lane == hl) {
-          double c = running + incl - static_cast<double>(s);
+          FF c = ff_add(running, ff_sub(incl, ff(s)));
           int lastp = -1;
           for (int j = 0; j < N; ++j) {
             if (x[j] > 0.0f) {
               lastp = e0 + j;
-              c += static_cast<double>(x[j]);
-              if (target < c) { tok = e0 + j; break; }
+              c = ff_add(c, x[j]);
+              if (ff_lt(target, c)) { tok = e0 + j; break; }
             }
           }
           if (tok < 0) tok = lastp;
@@ -396,7 +484,7 @@ __device__ int warp_ordered_draw(int n, int warp, int lane, Load load, WL wl, do
       found = tok;
       done = true;
     }
-    running += it;
+    running = ff_add(running, it);
   });
   if (!done) found = warp_max_i(last_pos);
   return found;
@@ -475,15 +563,12 @@ __device__ void load_and_scan(const KArgs& a, const RowCtx<E>& rc, E* sl, Scratc
   int bad = 0, abort_ = 0;
 
   auto scan_vec = [&](int v) {  // vector v of the slice
-    float x[N];
-    Fmt<E>::load(sl, v, x);
-    float vm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-      bad |= (x[j] != x[j]);
-      vm = fmaxf(vm, x[j]);
-    }
-    if (vm > best) {
+    bool nan;
+    const float vm = Fmt<E>::vec_max(sl, v, nan);
+    bad |= nan;
+    if (vm > best) {  // rare: the running max rises O(log n) times per thread
+      float x[N];
+      Fmt<E>::load(sl, v, x);
       best = vm;
 #pragma unroll
       for (int j = N - 1; j >= 0; --j)
@@ -552,7 +637,7 @@ __device__ void load_and_scan(const KArgs& a, const RowCtx<E>& rc, E* sl, Scratc
       fl |= sm.wi2[w];
     }
     Slot& s = C.mine(sm);
-    s.d[0] = bv;
+    s.d[0] = ff(bv);
     s.i[0] = bi;
     s.i[1] = fl;
   }
@@ -562,7 +647,7 @@ __device__ void load_and_scan(const KArgs& a, const RowCtx<E>& rc, E* sl, Scratc
     int bi = INT_MAX, fl = 0;
     for (int r = 0; r < C.cs; ++r) {
       const Slot* s = (&mir[r]);
-      const float v = static_cast<float>(s->d[0]);
+      const float v = s->d[0].hi;
       const int i = s->i[0];
       if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
       fl |= s->i[1];
@@ -579,33 +664,33 @@ __device__ void load_and_scan(const KArgs& a, const RowCtx<E>& rc, E* sl, Scratc
 // Leaves per-(rank, warp) totals in the mirror (d[1 + w] of each rank), for a
 // following cluster_ordered_draw with the same weights and no exchange between.
 template <typename E, typename WF>
-__device__ double cluster_weight_total(const RowCtx<E>& rc, Scratch& sm, Cluster& C, WF wf) {
+__device__ FF cluster_weight_total(const RowCtx<E>& rc, Scratch& sm, Cluster& C, WF wf) {
   constexpr int N = Fmt<E>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   auto wl = [&](float (&x)[N], int e0, int nvalid) {
 #pragma unroll
     for (int j = 0; j < N; ++j) x[j] = (j < nvalid) ? wf(x[j], rc.s0 + e0 + j) : 0.0f;
   };
-  const double wt = warp_ordered_total<N>(rc.L, warp, lane, smem_loader(rc), wl);
+  const FF wt = warp_ordered_total<N>(rc.L, warp, lane, smem_loader(rc), wl);
   if (lane == 0) sm.wtot[warp] = wt;
   __syncthreads();
   if (threadIdx.x == 0) {
     Slot& s = C.mine(sm);
-    double tot = 0.0;
+    FF tot = ff(0.0f);
     for (int w = 0; w < kWarps; ++w) {
       s.d[1 + w] = sm.wtot[w];
-      tot += sm.wtot[w];
+      tot = ff_add(tot, sm.wtot[w]);
     }
     s.d[0] = tot;
   }
   const Slot* mir = C.exchange(sm);
   if (threadIdx.x == 0) {
-    double z = 0.0;
-    for (int r = 0; r < C.cs; ++r) z += (&mir[r])->d[0];
+    FF z = ff(0.0f);
+    for (int r = 0; r < C.cs; ++r) z = ff_add(z, mir[r].d[0]);
     sm.bd[0] = z;
   }
   __syncthreads();
-  const double z = sm.bd[0];
+  const FF z = sm.bd[0];
   __syncthreads();
   return z;
 }
@@ -620,18 +705,19 @@ __device__ void cluster_ordered_draw(const RowCtx<E>& rc, Scratch& sm, Cluster& 
   constexpr int N = Fmt<E>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    double total = 0.0;
+    FF total = ff(0.0f);
     for (int r = 0; r < C.cs; ++r)
-      for (int w = 0; w < kWarps; ++w) total += (&mir[r])->d[1 + w];
-    const double target = u * total;
+      for (int w = 0; w < kWarps; ++w) total = ff_add(total, mir[r].d[1 + w]);
+    const FF target = ff_from_d(u * ff_to_d(total));
     int fr = -1, fw = -1, lr = 0, lw = 0;
-    double base = 0.0, cum = 0.0;
+    FF base = ff(0.0f), cum = ff(0.0f);
     for (int r = 0; r < C.cs && fr < 0; ++r)
       for (int w = 0; w < kWarps; ++w) {
-        const double t = (&mir[r])->d[1 + w];
-        if (t > 0.0) { lr = r; lw = w; }
-        if (target < cum + t) { fr = r; fw = w; base = cum; break; }
-        cum += t;
+        const FF t = mir[r].d[1 + w];
+        if (t.hi > 0.0f) { lr = r; lw = w; }
+        const FF next = ff_add(cum, t);
+        if (ff_lt(target, next)) { fr = r; fw = w; base = cum; break; }
+        cum = next;
       }
     const int overflow = fr < 0;
     if (overflow) { fr = lr; fw = lw; }
@@ -644,7 +730,7 @@ __device__ void cluster_ordered_draw(const RowCtx<E>& rc, Scratch& sm, Cluster& 
   __syncthreads();
   const int fr = sm.bi[0], fw = sm.bi[1];
   const bool overflow = sm.bi[2] != 0;
-  const double target = sm.bd[0], base = sm.bd[1];
+  const FF target = sm.bd[0], base = sm.bd[1];
   __syncthreads();
   if (C.rank == fr && warp == fw) {
     auto wl = [&](float (&x)[N], int e0, int nvalid) {
@@ -662,7 +748,7 @@ __device__ void cluster_ordered_draw(const RowCtx<E>& rc, Scratch& sm, Cluster& 
 template <typename E>
 __device__ void probe_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, const float (&thr)[kProbes], int np,
                            bool with_mass, bool restricted, Cut rcut, int (&cnt_out)[kProbes],
-                           double (&mass_out)[kProbes]) {
+                           FF (&mass_out)[kProbes]) {
   constexpr int N = Fmt<E>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int cnt[kProbes];
@@ -693,24 +779,24 @@ __device__ void probe_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, const f
     Slot& s = C.mine(sm);
     for (int p = 0; p < np; ++p) {
       int ct = 0;
-      double ms = 0.0;
-      for (int w = 0; w < kWarps; ++w) { ct += sm.pcnt[p][w]; ms += sm.pmass[p][w]; }
+      FF ms = ff(0.0f);
+      for (int w = 0; w < kWarps; ++w) { ct += sm.pcnt[p][w]; ms = ff_add(ms, sm.pmass[p][w]); }
       s.i[p] = ct;
       s.d[p] = ms;
     }
   }
   const Slot* mir = C.exchange(sm);
   if (threadIdx.x == 0) {
-    for (int p = 0; p < np; ++p) { sm.bi[p] = 0; sm.bd[p] = 0.0; }
+    for (int p = 0; p < np; ++p) { sm.bi[p] = 0; sm.bd[p] = ff(0.0f); }
     for (int r = 0; r < C.cs; ++r) {
       const Slot* s = (&mir[r]);
-      for (int p = 0; p < np; ++p) { sm.bi[p] += s->i[p]; sm.bd[p] += s->d[p]; }
+      for (int p = 0; p < np; ++p) { sm.bi[p] += s->i[p]; sm.bd[p] = ff_add(sm.bd[p], s->d[p]); }
     }
   }
   __syncthreads();
   for (int p = 0; p < kProbes; ++p) {
     cnt_out[p] = (p < np) ? sm.bi[p] : 0;
-    mass_out[p] = (p < np) ? sm.bd[p] : 0.0;
+    mass_out[p] = (p < np) ? sm.bd[p] : ff(0.0f);
   }
   __syncthreads();
 }
@@ -785,26 +871,31 @@ __device__ __forceinline__ int skey_idx(unsigned long long k) {
   return static_cast<int>(0xffffffffu - static_cast<uint32_t>(k & 0xffffffffull));
 }
 
-// Ordered draw over n list entries (index order), weights wf(i) in fp64: smallest i
-// with u*R < cumsum(i); overflow -> last positive entry.  Block-wide; returns the
-// entry position on all threads, or -1 if R == 0.
+// Ordered draw over n list entries (index order), weights wf(i) (float, >= 0),
+// prefix sums in float-float: smallest i with u*R < cumsum(i); overflow -> last
+// positive entry.  Block-wide; returns the entry position on all threads, or -1
+// if R == 0.
 template <typename WF>
 __device__ int list_ordered_draw(int n, double u, Scratch& sm, WF wf) {
   const int i0 = 2 * threadIdx.x, i1 = i0 + 1;  // n <= kCap = 2 * kThreads
-  const double w0 = (i0 < n) ? wf(i0) : 0.0;
-  const double w1 = (i1 < n) ? wf(i1) : 0.0;
-  double total;
-  const double excl = block_excl_scan_d(w0 + w1, &total, sm);
-  if (threadIdx.x == 0) { sm.bi[0] = INT_MAX; sm.bi[1] = -1; }
+  const float w0 = (i0 < n) ? wf(i0) : 0.0f;
+  const float w1 = (i1 < n) ? wf(i1) : 0.0f;
+  FF total;
+  const FF excl = block_excl_scan_ff(ff_add(ff(w0), w1), &total, sm);
+  if (threadIdx.x == 0) {
+    sm.bi[0] = INT_MAX;
+    sm.bi[1] = -1;
+    sm.bd[0] = ff_from_d(u * ff_to_d(total));
+  }
   __syncthreads();
   int r = -1;
-  if (total > 0.0) {
-    const double target = u * total;
-    const double c0 = excl + w0, c1 = c0 + w1;
-    if (w0 > 0.0 && target < c0 && target >= excl) atomicMin(&sm.bi[0], i0);
-    if (w1 > 0.0 && target < c1 && target >= c0) atomicMin(&sm.bi[0], i1);
-    if (w1 > 0.0) atomicMax(&sm.bi[1], i1);
-    else if (w0 > 0.0) atomicMax(&sm.bi[1], i0);
+  if (total.hi > 0.0f) {
+    const FF target = sm.bd[0];
+    const FF c0 = ff_add(excl, w0), c1 = ff_add(c0, w1);
+    if (w0 > 0.0f && ff_lt(target, c0) && !ff_lt(target, excl)) atomicMin(&sm.bi[0], i0);
+    if (w1 > 0.0f && ff_lt(target, c1) && !ff_lt(target, c0)) atomicMin(&sm.bi[0], i1);
+    if (w1 > 0.0f) atomicMax(&sm.bi[1], i1);
+    else if (w0 > 0.0f) atomicMax(&sm.bi[1], i0);
     __syncthreads();
     r = (sm.bi[0] != INT_MAX) ? sm.bi[0] : sm.bi[1];
   }
@@ -812,31 +903,235 @@ __device__ int list_ordered_draw(int n, double u, Scratch& sm, WF wf) {
   return r;
 }
 
-// ---- exact cut ----------------------------------------------------------------
-
 // Bracket [lo, hi) over data keys: pred(lo) holds, pred(hi) fails; counts and
 // masses are of the elements with key >= lo (resp. >= hi), restricted to rcut.
 struct Bracket {
   uint32_t lo, hi;
   int cnt_lo, cnt_hi;
-  double mass_lo, mass_hi;
+  FF mass_lo, mass_hi;
 };
 
-// Narrow until cnt_lo <= kCap (sortable on chip) or hi == lo + 1 (one key value).
-// pred = (mass_mode ? mass >= need_mass : count >= need_cnt).
+// ---- first pass ---------------------------------------------------------------
+// One sweep over the resident slice after the max is known.  It computes the
+// normaliser (when needed: no filter, or top-p without top-k), the counts and
+// masses of the elements above each of the first probe thresholds, and, per
+// warp, the index-ordered list of elements above the lowest threshold (up to
+// kWarpCap; more sets `overflow`).  One cluster exchange publishes everything.
+
+struct PassA {
+  FF z;
+  int cnt[kProbes];
+  FF mass[kProbes];
+  int overflow;
+};
+
+// First probe thresholds: m - W*scale on the data grid, strictly descending.
 template <typename E>
-__device__ Bracket bracket_search(const RowCtx<E>& rc, Scratch& sm, Cluster& C, bool mass_mode, int need_cnt,
-                                  double need_mass, float scale, bool restricted, Cut rcut, int cnt_all,
-                                  double mass_all) {
+__device__ int first_probes(float m, float scale, float (&thr)[kProbes]) {
+  const float W[kProbes] = {0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f, 8.f};
+  int np = 0;
+  uint32_t prev = Fmt<E>::key(m) + 1;
+  const uint32_t kmin = Fmt<E>::key(-INFINITY);
+  for (int j = 0; j < kProbes; ++j) {
+    const float t = Fmt<E>::round_to_grid(m - W[j] * scale);
+    if (!(t == t) || !(t > -INFINITY)) break;
+    uint32_t k = Fmt<E>::key(t);
+    if (k >= prev) k = prev - 1;
+    if (k <= kmin) break;
+    thr[np++] = Fmt<E>::val(k);
+    prev = k;
+  }
+  for (int j = np; j < kProbes; ++j) thr[j] = -INFINITY;
+  return np;
+}
+
+template <typename E>
+__device__ void first_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, bool need_z, bool filtered,
+                           bool with_mass, const float (&thr)[kProbes], int np, PassA& out) {
+  constexpr int N = Fmt<E>::N;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int cnt[kProbes];
+  float mass[kProbes];
+#pragma unroll
+  for (int p = 0; p < kProbes; ++p) { cnt[p] = 0; mass[p] = 0.0f; }
+  const float lowest = (filtered && np > 0) ? thr[np - 1] : INFINITY;
+  FF running = ff(0.0f);
+  int lcount = 0;  // warp-uniform list length
+  int32_t* widx = sm.cand_idx + warp * kWarpCap;
+  float* wval = sm.cand_val + warp * kWarpCap;
+  for_warp_segment<N>(rc.L, warp, lane, smem_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
+    if (need_z) {  // same arithmetic as warp_ordered_total with weights wexp
+      float s = 0.0f;
+#pragma unroll
+      for (int j = 0; j < N; ++j) s += (j < nvalid) ? wexp(x[j], rc.m, rc.c) : 0.0f;
+      running = ff_add(running, warp_sum_f(s));
+    }
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) c += (j < nvalid && x[j] >= lowest) ? 1 : 0;
+    if (__any_sync(FULL, c != 0)) {
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        if (j < nvalid && x[j] >= lowest) {
+          const float w = with_mass ? wexp(x[j], rc.m, rc.c) : 0.0f;
+#pragma unroll
+          for (int p = 0; p < kProbes; ++p)
+            if (p < np && x[j] >= thr[p]) { cnt[p] += 1; mass[p] += w; }
+        }
+      }
+      const int incl = warp_incl_scan_i(c, lane);
+      int pos = lcount + incl - c;
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        if (j < nvalid && x[j] >= lowest) {
+          if (pos < kWarpCap) { widx[pos] = rc.s0 + e0 + j; wval[pos] = x[j]; }
+          ++pos;
+        }
+      }
+      lcount += __shfl_sync(FULL, incl, 31);
+    }
+  });
+#pragma unroll
+  for (int p = 0; p < kProbes; ++p) {
+    cnt[p] = warp_sum_i(cnt[p]);
+    mass[p] = warp_sum_f(mass[p]);
+    if (lane == 0) { sm.pcnt[p][warp] = cnt[p]; sm.pmass[p][warp] = mass[p]; }
+  }
+  if (lane == 0) {
+    sm.wtot[warp] = running;
+    sm.wi2[warp] = min(lcount, kWarpCap);
+    sm.wi[warp] = lcount > kWarpCap;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Slot& s = C.mine(sm);
+    FF z = ff(0.0f);
+    int of = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      s.d[1 + w] = sm.wtot[w];
+      z = ff_add(z, sm.wtot[w]);
+      of |= sm.wi[w];
+    }
+    s.d[0] = z;
+    for (int p = 0; p < kProbes; ++p) {
+      int ct = 0;
+      FF ms = ff(0.0f);
+      for (int w = 0; w < kWarps; ++w) { ct += sm.pcnt[p][w]; ms = ff_add(ms, sm.pmass[p][w]); }
+      s.i[p] = ct;
+      s.d[1 + kWarps + p] = ms;
+    }
+    s.i[kProbes] = of;
+  }
+  const Slot* mir = C.exchange(sm);
+  // thread 0 reduces the mirror in rank order; the whole CTA reads the result
+  if (threadIdx.x == 0) {
+    FF z = ff(0.0f);
+    int of = 0;
+    for (int r = 0; r < C.cs; ++r) { z = ff_add(z, mir[r].d[0]); of |= mir[r].i[kProbes]; }
+    for (int p = 0; p < kProbes; ++p) {
+      int ct = 0;
+      FF ms = ff(0.0f);
+      for (int r = 0; r < C.cs; ++r) { ct += mir[r].i[p]; ms = ff_add(ms, mir[r].d[1 + kWarps + p]); }
+      sm.bi[p] = ct;
+      sm.bd[p] = ms;
+    }
+    sm.bd[kProbes] = z;
+    sm.bi[kProbes] = of;
+  }
+  __syncthreads();
+  out.z = sm.bd[kProbes];
+  out.overflow = sm.bi[kProbes];
+  for (int p = 0; p < kProbes; ++p) { out.cnt[p] = sm.bi[p]; out.mass[p] = sm.bd[p]; }
+  __syncthreads();
+}
+
+// Bracket implied by the first pass's probes (same update rule as bracket_search).
+template <typename E>
+__device__ Bracket bracket_from_probes(float m, const float (&thr)[kProbes], int np, const PassA& pa,
+                                       bool mass_mode, int need_cnt, FF need_mass, int cnt_all,
+                                       FF mass_all, int* first_true_out) {
   Bracket br;
   br.lo = Fmt<E>::key(-INFINITY);
-  br.hi = Fmt<E>::key(rc.m) + 1;
+  br.hi = Fmt<E>::key(m) + 1;
   br.cnt_lo = cnt_all;
   br.mass_lo = mass_all;
   br.cnt_hi = 0;
-  br.mass_hi = 0.0;
+  br.mass_hi = ff(0.0f);
+  int ft = -1;
+  for (int j = 0; j < np; ++j) {  // thr[0] is the largest threshold
+    const bool ok = mass_mode ? !ff_lt(pa.mass[j], need_mass) : (pa.cnt[j] >= need_cnt);
+    if (ok) { ft = j; break; }
+  }
+  if (ft >= 0) {
+    br.lo = Fmt<E>::key(thr[ft]);
+    br.cnt_lo = pa.cnt[ft];
+    br.mass_lo = pa.mass[ft];
+    if (ft > 0) {
+      br.hi = Fmt<E>::key(thr[ft - 1]);
+      br.cnt_hi = pa.cnt[ft - 1];
+      br.mass_hi = pa.mass[ft - 1];
+    }
+  } else if (np > 0) {
+    br.hi = Fmt<E>::key(thr[np - 1]);
+    br.cnt_hi = pa.cnt[np - 1];
+    br.mass_hi = pa.mass[np - 1];
+  }
+  *first_true_out = ft;
+  return br;
+}
+
+// After a CTA has its candidates at cand_*[0 .. n) in index order: publish n,
+// and rank 0 appends the other ranks' lists after its own in one flat round of
+// remote loads.  Returns the cluster count on every CTA.
+__device__ int rank0_collect(Scratch& sm, Cluster& C, int n) {
+  if (threadIdx.x == 0) C.mine(sm).i[0] = n;
+  const Slot* mir = C.exchange(sm);
+  int off[kMaxCluster + 1];
+  off[0] = 0;
+  for (int r = 0; r < C.cs; ++r) off[r + 1] = off[r] + mir[r].i[0];
+  const int total = off[C.cs];
+  if (C.rank == 0) {
+    for (int j = n + threadIdx.x; j < min(total, kCap); j += kThreads) {
+      int r = 1;
+      while (r + 1 < C.cs && j >= off[r + 1]) ++r;
+      const int i = j - off[r];
+      sm.cand_idx[j] = C.cl.map_shared_rank(sm.cand_idx, r)[i];
+      sm.cand_val[j] = C.cl.map_shared_rank(sm.cand_val, r)[i];
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
+// Candidates from the first pass's warp lists: keep entries >= lo_val, compact
+// them (warp order = index order) to the front, and collect them on rank 0.
+__device__ int lists_gather(Scratch& sm, Cluster& C, float lo_val) {
+  const int j0 = 2 * threadIdx.x, j1 = j0 + 1;  // 2 * kThreads == kCap slots
+  const int f0 = (j0 % kWarpCap) < sm.wi2[j0 / kWarpCap] && sm.cand_val[j0] >= lo_val;
+  const int f1 = (j1 % kWarpCap) < sm.wi2[j1 / kWarpCap] && sm.cand_val[j1] >= lo_val;
+  const int32_t i0 = sm.cand_idx[j0], i1 = sm.cand_idx[j1];
+  const float v0 = sm.cand_val[j0], v1 = sm.cand_val[j1];
+  int tot;
+  const int pos = block_excl_scan_i(f0 + f1, &tot, sm);
+  if (f0) { sm.cand_idx[pos] = i0; sm.cand_val[pos] = v0; }
+  if (f1) { sm.cand_idx[pos + f0] = i1; sm.cand_val[pos + f0] = v1; }
+  __syncthreads();
+  return rank0_collect(sm, C, tot);
+}
+
+// ---- exact cut ----------------------------------------------------------------
+
+
+// Narrow `br` until cnt_lo <= kCap (sortable on chip) or hi == lo + 1 (one key
+// value).  pred = (mass_mode ? mass >= need_mass : count >= need_cnt).  Unless
+// `probed` (a first pass already probed near the max), the first probes sit at
+// m - W*scale; later ones split [lo, hi) evenly in key space.
+template <typename E>
+__device__ Bracket bracket_search(const RowCtx<E>& rc, Scratch& sm, Cluster& C, bool mass_mode, int need_cnt,
+                                  FF need_mass, float scale, bool restricted, Cut rcut, Bracket br,
+                                  bool probed) {
   const float W[kProbes] = {0.5f, 1.f, 2.f, 3.f, 4.f, 6.f, 8.f, 16.f};
-  for (int pass = 0; pass < kMaxPasses; ++pass) {
+  for (int pass = probed ? 1 : 0; pass < kMaxPasses; ++pass) {
     if (br.cnt_lo <= kCap || br.hi - br.lo <= 1) break;
     uint32_t keys[kProbes];  // ascending, strictly inside (lo, hi)
     int np = 0;
@@ -865,12 +1160,12 @@ __device__ Bracket bracket_search(const RowCtx<E>& rc, Scratch& sm, Cluster& C, 
 #pragma unroll
     for (int j = 0; j < kProbes; ++j) thr[j] = (j < np) ? Fmt<E>::val(keys[np - 1 - j]) : 0.0f;
     int cnt[kProbes];
-    double mass[kProbes];
+    FF mass[kProbes];
     probe_pass<E>(rc, sm, C, thr, np, mass_mode, restricted, rcut, cnt, mass);
     // thr[j] is keys[np-1-j]: walk from the largest key down
     int first_true = -1;
     for (int j = 0; j < np; ++j) {
-      const bool ok = mass_mode ? (mass[j] >= need_mass) : (cnt[j] >= need_cnt);
+      const bool ok = mass_mode ? !ff_lt(mass[j], need_mass) : (cnt[j] >= need_cnt);
       if (ok) { first_true = j; break; }
     }
     if (first_true >= 0) {
@@ -900,24 +1195,7 @@ __device__ int gather_candidates(const RowCtx<E>& rc, Scratch& sm, Cluster& C, f
   const int n = cta_ordered_compact<E>(rc, sm, pred, [&](int pos, float l, int x) {
     if (pos < kCap) { sm.cand_idx[pos] = x; sm.cand_val[pos] = l; }
   });
-  if (threadIdx.x == 0) C.mine(sm).i[0] = n;
-  const Slot* mir = C.exchange(sm);
-  int off[kMaxCluster + 1];
-  off[0] = 0;
-  for (int r = 0; r < C.cs; ++r) off[r + 1] = off[r] + mir[r].i[0];
-  const int total = off[C.cs];
-  if (C.rank == 0) {
-    // one flat round of remote loads: position j comes from the rank whose range holds it
-    for (int j = n + threadIdx.x; j < min(total, kCap); j += kThreads) {
-      int r = 1;
-      while (r + 1 < C.cs && j >= off[r + 1]) ++r;
-      const int i = j - off[r];
-      sm.cand_idx[j] = C.cl.map_shared_rank(sm.cand_idx, r)[i];
-      sm.cand_val[j] = C.cl.map_shared_rank(sm.cand_val, r)[i];
-    }
-  }
-  __syncthreads();
-  return total;
+  return rank0_collect(sm, C, n);
 }
 
 // Rank 0 (all its threads): sort the n gathered candidates by (logit desc, index
@@ -927,9 +1205,9 @@ __device__ int gather_candidates(const RowCtx<E>& rc, Scratch& sm, Cluster& C, f
 // the cut index in sm.bi[1] and the gathered count in sm.bi[7].
 template <typename E>
 __device__ void rank0_sort_and_cut(const RowCtx<E>& rc, Scratch& sm, SortBuf sb, int n, int need_k, float top_p,
-                                   double z_for_p) {
+                                   FF z_for_p) {
   unsigned long long* skey = sb.skey;
-  double* scan = sb.scan;
+  FF* scan = sb.scan;
   int P = 1;
   while (P < n) P <<= 1;
   for (int i = threadIdx.x; i < P; i += kThreads)
@@ -940,27 +1218,27 @@ __device__ void rank0_sort_and_cut(const RowCtx<E>& rc, Scratch& sm, SortBuf sb,
   bitonic_sort_desc(skey, P);
   const int nk = (need_k > 0) ? min(need_k, n) : n;
   const int i0 = 2 * threadIdx.x, i1 = i0 + 1;
-  const double w0 = (i0 < nk) ? static_cast<double>(wexp(skey_val(skey[i0]), rc.m, rc.c)) : 0.0;
-  const double w1 = (i1 < nk) ? static_cast<double>(wexp(skey_val(skey[i1]), rc.m, rc.c)) : 0.0;
-  double total;
-  const double excl = block_excl_scan_d(w0 + w1, &total, sm);
-  if (i0 < nk) scan[i0] = excl + w0;
-  if (i1 < nk) scan[i1] = excl + w0 + w1;
+  const float w0 = (i0 < nk) ? wexp(skey_val(skey[i0]), rc.m, rc.c) : 0.0f;
+  const float w1 = (i1 < nk) ? wexp(skey_val(skey[i1]), rc.m, rc.c) : 0.0f;
+  FF total;
+  const FF excl = block_excl_scan_ff(ff_add(ff(w0), w1), &total, sm);
+  if (i0 < nk) scan[i0] = ff_add(excl, w0);
+  if (i1 < nk) scan[i1] = ff_add(ff_add(excl, w0), w1);
   if (threadIdx.x == 0) sm.bi[2] = INT_MAX;
   __syncthreads();
   int cut = nk - 1;
   if (top_p < 1.0f) {
-    const double zk = (need_k > 0) ? total : z_for_p;
-    const double need = static_cast<double>(top_p) * zk;
-    if (i0 < nk && scan[i0] >= need) atomicMin(&sm.bi[2], i0);
-    if (i1 < nk && scan[i1] >= need) atomicMin(&sm.bi[2], i1);
+    const FF zk = (need_k > 0) ? total : z_for_p;
+    const FF need = ff_mul(zk, top_p);
+    if (i0 < nk && !ff_lt(scan[i0], need)) atomicMin(&sm.bi[2], i0);
+    if (i1 < nk && !ff_lt(scan[i1], need)) atomicMin(&sm.bi[2], i1);
     __syncthreads();
     if (sm.bi[2] != INT_MAX) cut = sm.bi[2];  // otherwise rounding: keep all nk
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     sm.bd[0] = scan[cut];
-    sm.bd[1] = static_cast<double>(skey_val(skey[cut]));
+    sm.bd[1] = ff(skey_val(skey[cut]));
     sm.bi[0] = cut + 1;
     sm.bi[1] = skey_idx(skey[cut]);
     sm.bi[7] = n;  // gathered count (the kept list is filtered from these)
@@ -1033,7 +1311,7 @@ __device__ int tie_locate(const RowCtx<E>& rc, Scratch& sm, Cluster& C, float ti
 // order to lidx / lw.
 template <typename E>
 __device__ void kept_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, Cut cut, bool write_list, int32_t* lidx,
-                          float* lw, int* nkeep, double* zf, int* list_len) {
+                          float* lw, int* nkeep, FF* zf, int* list_len) {
   constexpr int N = Fmt<E>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   auto pred = [&](float l, int x) { return cut.keep(l, x); };
@@ -1042,25 +1320,25 @@ __device__ void kept_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, Cut cut,
     for (int j = 0; j < N; ++j)
       x[j] = (j < nvalid && cut.keep(x[j], rc.s0 + e0 + j)) ? wexp(x[j], rc.m, rc.c) : 0.0f;
   };
-  const double wt = warp_ordered_total<N>(rc.L, warp, lane, smem_loader(rc), wl);
+  const FF wt = warp_ordered_total<N>(rc.L, warp, lane, smem_loader(rc), wl);
   const int wc = warp_count<E>(rc, warp, lane, pred);
   if (lane == 0) { sm.wtot[warp] = wt; sm.wi2[warp] = wc; }
   __syncthreads();
   if (threadIdx.x == 0) {
     Slot& s = C.mine(sm);
-    double t = 0.0;
+    FF t = ff(0.0f);
     int ct = 0;
-    for (int w = 0; w < kWarps; ++w) { t += sm.wtot[w]; ct += sm.wi2[w]; }
+    for (int w = 0; w < kWarps; ++w) { t = ff_add(t, sm.wtot[w]); ct += sm.wi2[w]; }
     s.d[0] = t;
     s.i[0] = ct;
   }
   const Slot* mir = C.exchange(sm);
   if (threadIdx.x == 0) {
-    double z = 0.0;
+    FF z = ff(0.0f);
     int total = 0, off = 0;
     for (int r = 0; r < C.cs; ++r) {
       const Slot* s = (&mir[r]);
-      z += s->d[0];
+      z = ff_add(z, s->d[0]);
       if (r < C.rank) off += s->i[0];
       total += s->i[0];
     }
@@ -1153,24 +1431,25 @@ __device__ int global_rows_draw(const KArgs& a, const E* gt, const E* gd, float 
     for (int j = 0; j < N; ++j)
       if (j >= nvalid) x[j] = 0.0f;
   };
-  const double wt = warp_ordered_total<N, 4>(V, warp, lane, load, wl);
+  const FF wt = warp_ordered_total<N, 4>(V, warp, lane, load, wl);
   if (lane == 0) sm.wtot[warp] = wt;
   __syncthreads();
   if (threadIdx.x == 0) {
-    double total = 0.0;
-    for (int w = 0; w < kWarps; ++w) total += sm.wtot[w];
-    const double target = u * total;
+    FF total = ff(0.0f);
+    for (int w = 0; w < kWarps; ++w) total = ff_add(total, sm.wtot[w]);
+    const FF target = ff_from_d(u * ff_to_d(total));
     int fw = -1, lw = 0;
-    double base = 0.0, cum = 0.0;
+    FF base = ff(0.0f), cum = ff(0.0f);
     for (int w = 0; w < kWarps; ++w) {
-      const double t = sm.wtot[w];
-      if (t > 0.0) lw = w;
-      if (fw < 0 && target < cum + t) { fw = w; base = cum; }
-      cum += t;
+      const FF t = sm.wtot[w];
+      if (t.hi > 0.0f) lw = w;
+      const FF next = ff_add(cum, t);
+      if (fw < 0 && ff_lt(target, next)) { fw = w; base = cum; }
+      cum = next;
     }
     const int overflow = fw < 0;
     if (overflow) fw = lw;
-    sm.bi[0] = (total > 0.0) ? fw : -1;
+    sm.bi[0] = (total.hi > 0.0f) ? fw : -1;
     sm.bi[1] = overflow;
     sm.bd[0] = target;
     sm.bd[1] = base;
@@ -1179,7 +1458,7 @@ __device__ int global_rows_draw(const KArgs& a, const E* gt, const E* gd, float 
   __syncthreads();
   const int fw = sm.bi[0];
   const bool overflow = sm.bi[1] != 0;
-  const double target = sm.bd[0], base = sm.bd[1];
+  const FF target = sm.bd[0], base = sm.bd[1];
   if (fw >= 0 && warp == fw) {
     const int e = warp_ordered_draw<N, 4>(V, warp, lane, load, wl, target, base, overflow);
     if (lane == 0) sm.bi[2] = e;
@@ -1257,22 +1536,23 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
         for (int i = tid; i < ld; i += kThreads) { sm.cand_idx[i] = __ldcg(&di[i]); sm.cand_val[i] = __ldcg(&dw[i]); }
         __syncthreads();
       }
-      auto drf_w = [&](int x) -> double {
+      auto drf_w = [&](int x) -> float {
         int lo = 0, hi = ld;
         while (lo < hi) {
           const int mid = (lo + hi) >> 1;
           if (sm.cand_idx[mid] < x) lo = mid + 1; else hi = mid;
         }
-        return (lo < ld && sm.cand_idx[lo] == x) ? static_cast<double>(sm.cand_val[lo]) : 0.0;
+        return (lo < ld && sm.cand_idx[lo] == x) ? sm.cand_val[lo] : 0.0f;
       };
+      // residual max(0, tgt - drf) with the same float arithmetic as the full-row draw
+      const float izt = 1.0f / static_cast<float>(zt), izd = 1.0f / static_cast<float>(zd);
       int pos = -1;
       if (resid)
         pos = list_ordered_draw(lt, u, sm, [&](int i) {
-          const double r = static_cast<double>(__ldcg(&tw[i])) / zt - drf_w(__ldcg(&ti[i])) / zd;
-          return r > 0.0 ? r : 0.0;
+          return fmaxf(0.0f, __ldcg(&tw[i]) * izt - drf_w(__ldcg(&ti[i])) * izd);
         });
       if (pos < 0)  // bonus row, or zero residual mass: the target row itself
-        pos = list_ordered_draw(lt, u, sm, [&](int i) { return static_cast<double>(__ldcg(&tw[i])); });
+        pos = list_ordered_draw(lt, u, sm, [&](int i) { return __ldcg(&tw[i]); });
       token = (pos >= 0) ? __ldcg(&ti[pos]) : -1;
     } else {
       const E* gt = static_cast<const E*>(a.tgt) + (static_cast<int64_t>(b) * a.tgt_seq + static_cast<int64_t>(rt) * a.tgt_row);
@@ -1282,7 +1562,7 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
       const float mt = __ldcg(&recs[rt].m), md = resid ? __ldcg(&recs[rd].m) : 0.0f;
       const Cut ct{__ldcg(&recs[rt].tau_val), __ldcg(&recs[rt].tau_idx)};
       const Cut cd = resid ? Cut{__ldcg(&recs[rd].tau_val), __ldcg(&recs[rd].tau_idx)} : cut_all();
-      const float izt = static_cast<float>(1.0 / zt), izd = static_cast<float>(1.0 / zd);
+      const float izt = 1.0f / static_cast<float>(zt), izd = 1.0f / static_cast<float>(zd);
       token = -1;
       if (resid) token = global_rows_draw<E>(a, gt, gd, mt, md, ct, cd, izt, izd, true, u, sm);
       if (token < 0) token = global_rows_draw<E>(a, gt, gt, mt, mt, ct, ct, izt, izt, false, u, sm);
@@ -1304,7 +1584,7 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
   Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
   E* sl = reinterpret_cast<E*>(smem_raw + sizeof(Scratch));
   const SortBuf sb{reinterpret_cast<unsigned long long*>(sl),
-                   reinterpret_cast<double*>(reinterpret_cast<unsigned char*>(sl) + kCap * sizeof(unsigned long long))};
+                   reinterpret_cast<FF*>(reinterpret_cast<unsigned char*>(sl) + kCap * sizeof(unsigned long long))};
   const int tid = threadIdx.x;
   const int job = static_cast<int>(blockIdx.x) / C.cs;
   const RowInfo ri = decode_job(a, job);
@@ -1330,26 +1610,39 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
   const bool use_p = a.top_p < 1.0f;
 
   Cut cut = cut_all();
-  double zf = 1.0;
+  FF zf = ff(1.0f);
   int list_len = -1;
   bool rank0_list = false;  // kept list sits in rank 0's candidate arrays
 
   if (!bad && !a.greedy) {
-    auto wall = [&](float l, int) { return wexp(l, rc.m, rc.c); };
-    if (!use_k && !use_p) {
-      zf = cluster_weight_total<E>(rc, sm, C, wall);
+    // first pass: normaliser (no filter, or top-p without top-k), first probes and
+    // candidate lists (top-k by count, else top-p by mass)
+    const bool need_z = !use_k;
+    const bool filtered = use_k || use_p;
+    const bool mass_mode = !use_k;
+    float thr[kProbes];
+    const int np = filtered ? first_probes<E>(rc.m, use_k ? 1.0f : a.temp, thr) : 0;
+    PassA pa;
+    first_pass<E>(rc, sm, C, need_z, filtered, filtered && mass_mode, thr, np, pa);
+    if (!filtered) {
+      zf = pa.z;
     } else {
-      double zk = 0.0;
-      if (!use_k) zk = cluster_weight_total<E>(rc, sm, C, wall);
-      bool restricted = false;
+      FF zk = pa.z;
+      bool restricted = false, final_tie = false;
       Cut kcut = cut_all();
-      bool final_tie = false;
       if (use_k) {
         // stage A: top-k by count
-        const Bracket br = bracket_search<E>(rc, sm, C, false, a.top_k, 0.0, 1.0f, false, cut_all(), a.V, 0.0);
-        if (br.cnt_lo <= kCap) {
-          const int n = gather_candidates<E>(rc, sm, C, Fmt<E>::val(br.lo), false, cut_all());
-          if (C.rank == 0) rank0_sort_and_cut<E>(rc, sm, sb, n, a.top_k, use_p ? a.top_p : 1.0f, 0.0);
+        int ft;
+        Bracket br = bracket_from_probes<E>(rc.m, thr, np, pa, false, a.top_k, ff(0.0f), a.V, ff(0.0f), &ft);
+        int n = -1;
+        if (ft >= 0 && br.cnt_lo <= kCap && !pa.overflow) {
+          n = lists_gather(sm, C, Fmt<E>::val(br.lo));
+        } else {
+          br = bracket_search<E>(rc, sm, C, false, a.top_k, ff(0.0f), 1.0f, false, cut_all(), br, np > 0);
+          if (br.cnt_lo <= kCap) n = gather_candidates<E>(rc, sm, C, Fmt<E>::val(br.lo), false, cut_all());
+        }
+        if (n >= 0) {
+          if (C.rank == 0) rank0_sort_and_cut<E>(rc, sm, sb, n, a.top_k, use_p ? a.top_p : 1.0f, ff(0.0f));
           rank0_list = true;
         } else {
           const float tv = Fmt<E>::val(br.lo);
@@ -1361,26 +1654,40 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
       }
       if (use_p && !rank0_list) {
         // stage B: top-p by mass, within the top-k set when stage A ended in a tie cut
-        int cnt_all = a.V;
+        Bracket br;
+        int ft = -1;
         if (restricted) {
           int nk, ll;
           kept_pass<E>(rc, sm, C, kcut, false, nullptr, nullptr, &nk, &zk, &ll);
-          cnt_all = nk;
+          br.lo = Fmt<E>::key(-INFINITY);
+          br.hi = Fmt<E>::key(rc.m) + 1;
+          br.cnt_lo = nk;
+          br.mass_lo = zk;
+          br.cnt_hi = 0;
+          br.mass_hi = ff(0.0f);
+        } else {
+          br = bracket_from_probes<E>(rc.m, thr, np, pa, true, 0, ff_mul(zk, a.top_p), a.V, zk, &ft);
         }
-        const double need = static_cast<double>(a.top_p) * zk;
-        const Bracket br = bracket_search<E>(rc, sm, C, true, 0, need, a.temp, restricted, kcut, cnt_all, zk);
-        if (br.cnt_lo <= kCap) {
-          const int n = gather_candidates<E>(rc, sm, C, Fmt<E>::val(br.lo), restricted, kcut);
+        const FF need = ff_mul(zk, a.top_p);
+        int n = -1;
+        if (!restricted && ft >= 0 && br.cnt_lo <= kCap && !pa.overflow) {
+          n = lists_gather(sm, C, Fmt<E>::val(br.lo));
+        } else {
+          br = bracket_search<E>(rc, sm, C, true, 0, need, a.temp, restricted, kcut, br, !restricted && np > 0);
+          if (br.cnt_lo <= kCap) n = gather_candidates<E>(rc, sm, C, Fmt<E>::val(br.lo), restricted, kcut);
+        }
+        if (n >= 0) {
           if (C.rank == 0) rank0_sort_and_cut<E>(rc, sm, sb, n, 0, a.top_p, zk);
           rank0_list = true;
         } else {
           const float tv = Fmt<E>::val(br.lo);
-          const double w = static_cast<double>(wexp(tv, rc.m, rc.c));
+          const float w = wexp(tv, rc.m, rc.c);
           const int ties = br.cnt_lo - br.cnt_hi;
           int c = ties;
-          if (w > 0.0) {
-            const double k = ceil((need - br.mass_hi) / w);
-            c = static_cast<int>(fmin(fmax(k, 1.0), static_cast<double>(ties)));
+          if (w > 0.0f) {  // smallest c with mass_hi + c * w >= need
+            const FF rem = ff_sub(need, br.mass_hi);
+            const float k = ceilf((rem.hi + rem.lo) / w);
+            c = static_cast<int>(fminf(fmaxf(k, 1.0f), static_cast<float>(ties)));
           }
           const int ti = tie_locate<E>(rc, sm, C, tv, c, restricted, kcut);
           cut = Cut{tv, ti};
@@ -1396,15 +1703,15 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
 
   // rank 0: the kept list = gathered candidates (index order) kept by the cut
   if (rank0_list && C.rank == 0) {
-    cut = Cut{static_cast<float>(sm.bd[1]), sm.bi[1]};
+    cut = Cut{sm.bd[1].hi, sm.bi[1]};
     zf = sm.bd[0];
     list_len = sm.bi[0];
     const int gathered = sm.bi[7];
     const int i0 = 2 * tid, i1 = i0 + 1;
     const int f0 = (i0 < gathered) && cut.keep(sm.cand_val[i0], sm.cand_idx[i0]);
     const int f1 = (i1 < gathered) && cut.keep(sm.cand_val[i1], sm.cand_idx[i1]);
-    double tot;
-    const int pos = static_cast<int>(block_excl_scan_d(static_cast<double>(f0 + f1), &tot, sm));
+    int tot;
+    const int pos = block_excl_scan_i(f0 + f1, &tot, sm);
     if (f0) { lidx[pos] = sm.cand_idx[i0]; lw[pos] = wexp(sm.cand_val[i0], rc.m, rc.c); }
     if (f1) { lidx[pos + f0] = sm.cand_idx[i1]; lw[pos + f0] = wexp(sm.cand_val[i1], rc.m, rc.c); }
     __syncthreads();
@@ -1425,7 +1732,7 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
       if (!rank0_list) { __threadfence(); }
       C.cl.sync();  // lists written by every CTA are visible after the barrier
       if (C.rank == 0) {
-        const int pos = list_ordered_draw(list_len, u, sm, [&](int i) { return static_cast<double>(__ldcg(&lw[i])); });
+        const int pos = list_ordered_draw(list_len, u, sm, [&](int i) { return __ldcg(&lw[i]); });
         if (tid == 0) {
           const int tok = (pos >= 0) ? __ldcg(&lidx[pos]) : -1;
           *outp = tok;
@@ -1455,11 +1762,11 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
         flags |= kFlagToken;
       } else if (!bad && !a.greedy) {
         const float ld = Fmt<E>::at_global(rc.g, d);
-        if (cut.keep(ld, d) && ld > -INFINITY)
-          p_tok = exp((static_cast<double>(ld) - static_cast<double>(rc.m)) / static_cast<double>(a.temp)) / zf;
+        // same weight as the kept list and the normaliser use
+        if (cut.keep(ld, d) && ld > -INFINITY) p_tok = static_cast<double>(wexp(ld, rc.m, rc.c)) / ff_to_d(zf);
       }
     }
-    rec->zf = zf;
+    rec->zf = ff_to_d(zf);
     rec->p_tok = p_tok;
     rec->m = rc.m;
     rec->tau_val = cut.tv;
