@@ -25,9 +25,11 @@
  *   - Every buffer is owned by the caller.  Device pointers must stay valid
  *     until the work queued on params->stream has finished.  The library
  *     allocates no device memory per call: it needs a caller-provided
- *     workspace (see *_workspace_size) whose contents need no initialisation
- *     (per-call tags mark stale values).  Calls that share one workspace must
- *     not overlap in time on the GPU.
+ *     workspace (see *_workspace_size) that is zero-filled once before its
+ *     first use (cudaMemset).  Its first 64 KB hold the per-call counters;
+ *     every call leaves them at zero again, so a workspace is reused across
+ *     calls of any shape without clearing.  Calls that share one workspace
+ *     must not overlap in time on the GPU.
  *   - Calls are asynchronous on params->stream (a cudaStream_t; NULL = the
  *     legacy default stream).  Argument errors are detected on the host,
  *     returned synchronously, and nothing is launched.
@@ -65,8 +67,10 @@ typedef enum {
   SPEC_ERR_CUDA = 2,         /* host: a CUDA runtime call failed (launch, attribute) */
   SPEC_ERR_NONFINITE = 3,    /* device: NaN or +inf logit, or no finite logit, in a row read */
   SPEC_ERR_TOKEN_RANGE = 4,  /* device: a draft token outside [0, V) */
-  SPEC_ERR_TIMEOUT = 5,      /* device: a bounded wait on an asynchronous copy ran out */
-  SPEC_ERR_UNSUPPORTED = 6,  /* host: V too large for one row per thread-block cluster */
+  SPEC_ERR_TIMEOUT = 5,      /* device: reserved; a bulk copy that misses its bounded wait is
+                                replaced by plain loads, so this version never reports it */
+  SPEC_ERR_UNSUPPORTED = 6,  /* host: more shared memory than the device offers, or more than
+                                2^31 - 1 row segments in one call */
   SPEC_ERR_SCRATCH_LIMIT = 7 /* host: spec_verify_noalloc asked for more than its fixed scratch */
 } spec_status;
 
@@ -89,7 +93,7 @@ typedef struct {
   int32_t greedy;            /* nonzero: argmax special case (uniforms and draft rows unused) */
   void* stream;              /* cudaStream_t */
   int32_t* status;           /* optional device int32[1]: first device-detected error */
-  void* workspace;           /* device, 256-byte aligned, any contents */
+  void* workspace;           /* device, 256-byte aligned, zero-filled before first use */
   size_t workspace_bytes;
 } spec_params;
 
@@ -157,8 +161,10 @@ spec_status spec_sample_draft(const void* draft_logits, const double* uniforms,
 spec_status spec_read_row_stats(const spec_params* params, int32_t is_verify,
                                 spec_row_stat* host_out, int64_t max_rows);
 
-/* Scratch size of spec_verify_noalloc: 8 MiB, enough for about 2000 rows
- * (B * (2K+1) sampling, B * (K+1) greedy). */
+/* Scratch size of spec_verify_noalloc: 8 MiB.  Rows per call (B * (2K+1)
+ * sampling, B * (K+1) greedy) that fit: about 1900 greedy; sampling, about 800
+ * at V = 32000 and 150 at V = 256000 (bf16; every 24 KB segment of a row
+ * keeps a candidate list). */
 #define SPEC_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* spec_verify for callers that cannot allocate device memory.  Not a step of
@@ -180,8 +186,8 @@ spec_status spec_read_row_stats(const spec_params* params, int32_t is_verify,
  * device address once; make that first call before any stream capture.
  *
  *   - Every call uses the same array, which keeps the last call's contents.
- *     Nothing in it has to start at zero (the per-sequence counters carry a
- *     per-call tag), so no clearing is needed between calls.
+ *     The array starts zeroed and every call leaves its counters at zero, so
+ *     no clearing is needed between calls.
  *   - Calls whose work overlaps on the GPU (other streams, other threads)
  *     share the array and race: serialise them.
  *   - Returns SPEC_ERR_SCRATCH_LIMIT, with nothing launched, when

@@ -7,26 +7,32 @@
 // the FDE Interviews breakdown of that paper, section "01 The paper in one
 // minute".
 //
-// Design (one launch per call):
-//   * Every vocabulary row the method reads is one job.  A job runs on a
-//     thread-block cluster of CS CTAs; CTA r holds elements [r*S, r*S + S) of
-//     the row in shared memory, brought in by bulk asynchronous copies
-//     (cp.async.bulk + mbarrier) in up to four stages, scanned for the max as
-//     the stages land.  The row is read from HBM once; every later pass reads
-//     shared memory.
-//   * Row statistics (max, argmax, normaliser) and the top-k / top-p cut are
-//     reduced across the cluster through distributed shared memory.  Every CTA
-//     reduces the published per-CTA values in rank order, so all CTAs hold
-//     bit-identical results and take identical branches.
-//   * The cut is exact: an 8-probe bracket search over the order-preserving
-//     key of the logits narrows [lo, hi) until the elements >= lo fit the
-//     on-chip sort (<= kCap, by (logit desc, index asc)), or until the bracket
-//     holds a single key value, whose tie group is cut by index.
-//   * Each row writes a record (normaliser, cut, draft-token probability, the
-//     kept set in index order when it fits) to the caller's workspace.  The
-//     last cluster of a sequence to finish (atomic ticket, no spinning) runs
-//     the accept tests and the one final draw for that sequence.
-#include <cooperative_groups.h>
+// Design (one launch per call; no thread block ever waits for another):
+//   * Every vocabulary row the call reads is cut into equal segments of at
+//     most 12 K bf16 / 6 K fp32 elements (24 KB), one CTA per segment.  Each
+//     thread issues its sixteen 16-byte loads at once (64 KB in flight per CTA,
+//     every warp load 512 contiguous bytes) and keeps the values in registers:
+//     each byte of a row is read from HBM once and every later pass over the
+//     segment reads registers.
+//   * Per segment: max (NaN-propagating) and first argmax; the normaliser
+//     relative to the segment max when the row needs the full sum (no filter,
+//     or top-p without top-k); for top-k / top-p a candidate superset: theta =
+//     the n0-th largest of the 256 per-thread maxima, so that at least n0 of
+//     the segment's elements -- among them its top n0 -- lie at or above it,
+//     and every finite element >= theta goes to the segment's candidate list.
+//   * The CTA that finishes a row's last segment (tagged atomic ticket) merges
+//     the segment records: row max and argmax, normaliser (float-float, each
+//     segment rescaled to the row max) and the candidate pool, which is sorted
+//     by (logit desc, index asc) and cut: top-k exactly (each segment kept its
+//     own top-k), top-p when the cut value is >= every segment's theta (nothing
+//     a segment left out can then be kept).  Otherwise -- a pool overflow or a
+//     failed check -- the exact general path runs over the row in global
+//     memory: an 8-probe bracket search over order-preserving keys, ending in
+//     an on-chip sort or a tie cut by index.
+//   * The row record (normaliser, cut, draft-token probability, the kept set in
+//     index order) goes to the caller's workspace; the CTA that finishes a
+//     sequence's last row (second ticket) runs the accept tests and the one
+//     final draw for that sequence.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,21 +46,22 @@
 
 #include "spec_verify.h"
 
-namespace cg = cooperative_groups;
-
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCap = 512;       // on-chip sort capacity == stored kept-list capacity
-constexpr int kWarpCap = kCap / 8;  // first-pass candidate list per warp (8 warps)
 constexpr int kProbes = 8;      // thresholds evaluated per probe pass
-constexpr int kStages = 4;      // bulk-copy stages per slice
-constexpr int kMaxCluster = 8;  // portable cluster size
+constexpr int kPool = 1024;     // row candidate pool (shared memory), sorted at the row merge
+constexpr int kSegCap = 256;    // candidates one segment may contribute
+constexpr int kListTable = 4096; // listed entries a row merge can index (one byte each)
+constexpr size_t kCounterArea = 64 * 1024;  // workspace bytes kept zeroed between calls
+constexpr int kNV = 12;         // 16-byte vectors of a segment per thread (24 KB per segment)
 constexpr int kMaxPasses = 40;  // bound on probe passes (16-bit keys need <= 6, 32-bit <= 11)
 constexpr unsigned FULL = 0xffffffffu;
 
 constexpr int kFlagNonfinite = 1, kFlagToken = 2, kFlagTimeout = 4;
+constexpr int kSegBad = 1, kSegOver = 2;  // segment record flags
 
 enum { kModeVerify = 0, kModeSample = 1 };
 
@@ -99,13 +106,18 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait on phase 0 of a stage barrier: gives up after ~2 s of wall time
-// (and after a hard iteration cap), so a lost copy cannot hang the GPU.
-__device__ bool mbar_wait_bounded(uint64_t* bar) {
-  if (mbar_try_wait(bar, 0)) return true;
+// Order this CTA's generic-proxy accesses of shared memory before later bulk
+// copies (async proxy) into it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Bounded wait for the phase with the given parity: gives up after ~2 s of wall
+// time (and a hard iteration cap), so a lost copy cannot hang the GPU.
+__device__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0; it < 100000u; ++it) {
-    if (mbar_try_wait(bar, 0)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - t0 > 2000000000ull) break;
   }
   return false;
@@ -131,6 +143,14 @@ struct Fmt<float> {
     x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
   }
   __device__ static float at(const float* s, int64_t e) { return s[e]; }
+  // vector v of a row in global memory of length L (scalar loads at the tail or
+  // when the row start is not 16-byte aligned)
+  __device__ static void load_row(const float* g, int v, int L, bool aligned, float (&x)[4]) {
+    const int e0 = v * 4;
+    if (aligned && e0 + 4 <= L) { load_global(g, v, x); return; }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = (e0 + j < L) ? __ldg(g + e0 + j) : -INFINITY;
+  }
   // max of vector v (NaN-propagating) and whether it holds a NaN
   __device__ static float vec_max(const float* s, int v, bool& nan) {
     const float4 q = reinterpret_cast<const float4*>(s)[v];
@@ -171,6 +191,13 @@ struct Fmt<uint16_t> {  // bf16 carried as raw bits
     unpack(__ldg(reinterpret_cast<const uint4*>(g) + v), x);
   }
   __device__ static float at(const uint16_t* s, int64_t e) { return bf16_bits_to_float(s[e]); }
+  __device__ static void load_row(const uint16_t* g, int v, int L, bool aligned, float (&x)[8]) {
+    const int e0 = v * 8;
+    if (aligned && e0 + 8 <= L) { load_global(g, v, x); return; }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      x[j] = (e0 + j < L) ? bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(g) + e0 + j)) : -INFINITY;
+  }
   // max of vector v (NaN-propagating, on packed bf16 pairs) and whether it holds a NaN
   __device__ static float vec_max(const uint16_t* s, int v, bool& nan) {
     const uint4 q = reinterpret_cast<const uint4*>(s)[v];
@@ -250,12 +277,22 @@ __device__ __forceinline__ FF ff_from_d(double d) {
 __device__ __forceinline__ FF shfl_up_ff(FF v, int o) {
   return FF{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
 }
-__device__ __forceinline__ FF shfl_ff(FF v, int src) {
-  return FF{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
-}
 
 // ---------------------------------------------------------------------------
 // kernel arguments and shared scratch
+
+// What one segment leaves for its row's merge.
+struct SegRec {
+  float m;          // segment max (NaN / +inf: see flags)
+  int32_t argmax;   // first index of m in the row
+  float z_hi, z_lo; // sum of 2^((l - m) c) over the segment (when the row needs it)
+  float theta;      // candidate floor: every finite element >= theta was a candidate
+  float kth;        // top-k: the segment's k-th largest value (-inf if it has fewer)
+  int32_t ncand;    // listed candidates (<= kSegCap; top-k: the segment's top k)
+  int32_t flags;    // kSegBad, kSegOver
+  int32_t off;      // merge scratch: offset of this segment's candidates in the pool
+  int32_t pad_[3];
+};
 
 struct KArgs {
   const void* tgt;
@@ -266,25 +303,31 @@ struct KArgs {
   int32_t* out_tokens;
   int32_t* out_n;
   int32_t* status;
-  unsigned long long* tickets;  // [B]: (call tag << 32) | rows finished
-  uint32_t tag;                 // nonzero, distinct for consecutive calls
-  spec_row_stat* rows;  // [B * R]
-  int32_t* list_idx;    // [B * R * kCap]
-  float* list_w;        // [B * R * kCap]
-  int B, K, V, R, S;    // R rows per sequence, S slice elements per CTA
+  unsigned long long* tickets;  // counter area: [B] sequences, [nrows] rows, [1] work counter
+  spec_row_stat* rows;  // [nrows]
+  int32_t* list_idx;    // [nrows * kCap]
+  float* list_w;        // [nrows * kCap]
+  SegRec* segs;         // [nrows * nseg]
+  uint2* seg_cand;      // [nrows * nseg * kSegCap]: (row index, logit bits)
+  int B, K, V, R;       // R rows per sequence
+  int S, nseg, nrows;   // S elements per segment (a multiple of the vector width)
+  int seg_bytes;        // bytes of one segment buffer in shared memory
   int mode, greedy, top_k, aligned;
+  int need_z;           // segments sum the normaliser (no filter, or top-p without top-k)
+  int filt, n0;         // segments list candidates; theta is the n0-th thread maximum
   float top_p, c, temp;
 };
 
-struct Slot {  // per-CTA values published to the cluster
+struct Slot {  // values published by exchange()
   FF d[kProbes + kWarps + 4];
   int32_t i[kProbes + kWarps + 4];
 };
 
 struct alignas(128) Scratch {
-  uint64_t bar[kStages];
+  uint64_t bar[2];     // completion of each segment buffer's bulk copy
+  int32_t items[4];    // item of iteration k at [k & 3]; nitems = none
+  int32_t issued[2];   // a bulk copy is in flight into the buffer
   Slot slot[2];
-  Slot mirror[kMaxCluster];  // local copy of every rank's slot after an exchange
   // block-level reduction scratch
   float wf[kWarps];
   int32_t wi[kWarps];
@@ -293,26 +336,33 @@ struct alignas(128) Scratch {
   int32_t pcnt[kProbes][kWarps];
   float pmass[kProbes][kWarps];
   FF wtot[kWarps];
-  // values broadcast to the whole CTA by thread 0
-  float m;
-  int32_t argmax, bad, abort_;
+  // segment phase
+  alignas(16) float tmax[kThreads];  // per-thread maxima (read as float4)
+  float theta, kth;
+  int32_t seg_n, last;
+  // the row being merged
+  FF row_z;
+  float row_m, row_theta, row_kth;
+  int32_t row_argmax, row_flags, row_over, pool_n;
   FF bd[kProbes + 4];
   int32_t bi[kProbes + 8];
-  // candidates: this CTA's, and on rank 0 the cluster's gathered list
+  // candidates of the general path; the draft's kept list in the epilogue
   int32_t cand_idx[kCap];
   float cand_val[kCap];
 };
 
-// Rank 0's sort buffers live in its slice buffer: on the path that sorts, the
-// slice is no longer read once the candidates are gathered.
+// Sort keys of the row merge (in the consumed segment buffer, after the pool).
 struct SortBuf {
-  unsigned long long* skey;  // [kCap]
-  FF* scan;                  // [kCap]
+  unsigned long long* skey;  // [kPool]
 };
-constexpr size_t kSortBufBytes = kCap * (sizeof(unsigned long long) + sizeof(FF));
-// scratch + a 64 KB slice must leave room for three CTAs in an SM's 228 KB
 static_assert(sizeof(Scratch) <= 8192, "shared scratch grew past its budget");
+static_assert(kCap % kThreads == 0 && kPool % kThreads == 0, "lists are split evenly over the threads");
+static_assert(kSegCap <= kCap, "a segment's candidates are staged in the candidate arrays");
+static_assert(sizeof(SegRec) % 16 == 0, "segment records are moved as 16-byte words");
 static_assert(sizeof(Slot) % sizeof(uint32_t) == 0, "slots are copied as 32-bit words");
+static_assert(kThreads * sizeof(SegRec) <= kPool * sizeof(unsigned long long),
+              "a tile of segment records is staged in the sort-key buffer");
+static_assert(kThreads <= 255, "the row merge's entry table stores segment numbers in one byte");
 
 // ---------------------------------------------------------------------------
 // warp / block helpers
@@ -491,36 +541,117 @@ __device__ int warp_ordered_draw(int n, int warp, int lane, Load load, WL wl, FF
 }
 
 // ---------------------------------------------------------------------------
-// cluster exchange.  Thread 0 (or one lane) fills sm.slot[C.ph] first;
-// exchange() is a cluster barrier (release/acquire), after which all threads copy
-// every rank's slot of that phase into the local mirror at once -- one round of
-// distributed-shared-memory loads instead of a serial chain -- and return it.
-// Slots alternate between two buffers, so a rank may overwrite its slot for the
-// next exchange while others still copy the previous one.  The mirror stays
-// valid until the next exchange().  Every thread tracks the phase itself.
+// block exchange.  Thread 0 (or one lane) fills sm.slot[C.ph]; exchange() is a
+// block barrier after which every thread may read that slot, until the next
+// exchange().  Slots alternate, so the next writer never races a late reader.
+// The selection code below is written against this interface; here every
+// reduction is within one CTA (cs = 1, rank = 0).
 
-struct Cluster {
-  cg::cluster_group cl;
-  int cs, rank, ph;
-  __device__ Cluster() : cl(cg::this_cluster()), ph(0) {
-    cs = static_cast<int>(cl.num_blocks());
-    rank = static_cast<int>(cl.block_rank());
-  }
+struct Local {
+  static constexpr int cs = 1, rank = 0;
+  int ph = 0;
   __device__ Slot& mine(Scratch& sm) { return sm.slot[ph]; }
   __device__ const Slot* exchange(Scratch& sm) {
     const int p = ph;
-    cl.sync();
-    ph ^= 1;
-    constexpr int W = static_cast<int>(sizeof(Slot) / sizeof(uint32_t));
-    for (int i = threadIdx.x; i < cs * W; i += kThreads) {
-      const int r = i / W, o = i - r * W;
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(cl.map_shared_rank(&sm.slot[p], r));
-      reinterpret_cast<uint32_t*>(&sm.mirror[r])[o] = src[o];
-    }
     __syncthreads();
-    return sm.mirror;
+    ph ^= 1;
+    return &sm.slot[p];
   }
 };
+
+// ---------------------------------------------------------------------------
+// bitonic sorts of 64-bit keys held in registers (descending).  Key i sits in
+// thread i / R, slot i % R: exchanges at distance j < R stay in a thread, at
+// R <= j < 32 R go through lane shuffles, and only the wider ones (block sort)
+// through shared memory, stored slot-major so a warp's accesses are
+// conflict-free.
+
+__device__ __forceinline__ void cmp_desc(unsigned long long& a, unsigned long long& b, bool desc) {
+  const bool sw = desc ? (a < b) : (a > b);
+  const unsigned long long x = sw ? b : a, y = sw ? a : b;
+  a = x;
+  b = y;
+}
+
+// One in-thread stage (k, J) for the keys of thread t (J < R, so slot r pairs
+// with slot r | J; J is a compile-time constant so the keys stay in registers).
+template <int R, int J>
+__device__ __forceinline__ void sort_stage_regs_j(unsigned long long (&key)[R], int t, int k) {
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if ((r & J) == 0) cmp_desc(key[r], key[r | J], ((t * R + r) & k) == 0);
+}
+template <int R>
+__device__ __forceinline__ void sort_stage_regs(unsigned long long (&key)[R], int t, int k, int j) {
+  if (j == 1) {
+    if constexpr (R > 1) sort_stage_regs_j<R, 1>(key, t, k);
+  } else if (j == 2) {
+    if constexpr (R > 2) sort_stage_regs_j<R, 2>(key, t, k);
+  } else if (j == 4) {
+    if constexpr (R > 4) sort_stage_regs_j<R, 4>(key, t, k);
+  }
+  static_assert(R == 1 || R == 2 || R == 4 || R == 8, "keys per thread: 1, 2, 4 or 8");
+}
+template <int R>
+__device__ __forceinline__ void sort_stage_lanes(unsigned long long (&key)[R], int t, int k, int j) {
+  const int lx = j / R;
+  const bool lower = (t & lx) == 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const unsigned long long o = __shfl_xor_sync(FULL, key[r], lx);
+    const bool keep_max = (((t * R + r) & k) == 0) == lower;
+    key[r] = keep_max ? (key[r] > o ? key[r] : o) : (key[r] < o ? key[r] : o);
+  }
+}
+
+// 32 R keys in one warp.
+template <int R>
+__device__ void warp_sort_keys_desc(unsigned long long (&key)[R], int lane) {
+  for (int k = 2; k <= 32 * R; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < R) sort_stage_regs<R>(key, lane, k, j);
+      else sort_stage_lanes<R>(key, lane, k, j);
+    }
+}
+
+// kThreads * R keys over the whole block; xbuf holds kThreads * R keys.
+template <int R>
+__device__ void block_sort_keys_desc(unsigned long long (&key)[R], unsigned long long* xbuf) {
+  const int t = threadIdx.x;
+  for (int k = 2; k <= kThreads * R; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < R) {
+        sort_stage_regs<R>(key, t, k, j);
+      } else if (j < 32 * R) {
+        sort_stage_lanes<R>(key, t, k, j);
+      } else {
+        const int tx = j / R;
+        const bool lower = (t & tx) == 0;
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < R; ++r) xbuf[r * kThreads + t] = key[r];
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const unsigned long long o = xbuf[r * kThreads + (t ^ tx)];
+          const bool keep_max = (((t * R + r) & k) == 0) == lower;
+          key[r] = keep_max ? (key[r] > o ? key[r] : o) : (key[r] < o ? key[r] : o);
+        }
+      }
+    }
+  __syncthreads();
+}
+
+// Float-float sum over a warp (xor butterfly: every lane gets the same total).
+__device__ __forceinline__ FF warp_sum_ff(FF v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    v = ff_add(v, FF{__shfl_xor_sync(FULL, v.hi, o), __shfl_xor_sync(FULL, v.lo, o)});
+  return v;
+}
+
+// Sort key (value desc, index asc) of a logit: larger keys first.
+__device__ __forceinline__ unsigned long long sort_key(float v, int idx);
 
 // ---------------------------------------------------------------------------
 // per-row state
@@ -534,9 +665,11 @@ struct RowInfo {
 template <typename E>
 struct RowCtx {
   const E* g;   // row in global memory
-  const E* sl;  // this CTA's slice in shared memory
-  int s0, L;    // slice start (row index) and length
+  const E* sl;  // the data the passes read: the chunk in shared memory, or the row
+  int s0, L;    // first row index held in sl, and length
   float m, c;
+  int gsrc;     // sl is the row in global memory (general path of a row merge)
+  int aligned;  // global row start is 16-byte aligned
 };
 
 // The kept set as a prefix of the (logit desc, index asc) order:
@@ -549,204 +682,18 @@ struct Cut {
 __device__ __forceinline__ Cut cut_all() { return Cut{-INFINITY, INT_MAX}; }
 
 template <typename E>
-__device__ __forceinline__ auto smem_loader(const RowCtx<E>& rc) {
-  return [&rc](int v, float (&x)[Fmt<E>::N]) { Fmt<E>::load(rc.sl, v, x); };
-}
-
-// ---- load + max/argmax/non-finite scan --------------------------------------
-template <typename E>
-__device__ void load_and_scan(const KArgs& a, const RowCtx<E>& rc, E* sl, Scratch& sm, Cluster& C) {
-  constexpr int N = Fmt<E>::N;
-  const int tid = threadIdx.x;
-  float best = -INFINITY;
-  int best_idx = INT_MAX;
-  int bad = 0, abort_ = 0;
-
-  auto scan_vec = [&](int v) {  // vector v of the slice
-    bool nan;
-    const float vm = Fmt<E>::vec_max(sl, v, nan);
-    bad |= nan;
-    if (vm > best) {  // rare: the running max rises O(log n) times per thread
-      float x[N];
-      Fmt<E>::load(sl, v, x);
-      best = vm;
-#pragma unroll
-      for (int j = N - 1; j >= 0; --j)
-        if (x[j] == vm) best_idx = rc.s0 + v * N + j;
-    }
+__device__ __forceinline__ auto row_loader(const RowCtx<E>& rc) {
+  return [&rc](int v, float (&x)[Fmt<E>::N]) {
+    if (rc.gsrc) Fmt<E>::load_row(rc.sl, v, rc.L, rc.aligned != 0, x);
+    else Fmt<E>::load(rc.sl, v, x);
   };
-
-  const int64_t bytes = static_cast<int64_t>(rc.L) * sizeof(E);
-  const int64_t bulk = a.aligned ? (bytes & ~int64_t(15)) : 0;
-  int nst = 0;
-  int64_t chunk = 0;
-  if (bulk > 0) {
-    nst = static_cast<int>((bulk / 16 < kStages ? bulk / 16 : int64_t(kStages)));
-    chunk = ((bulk / nst) + 15) & ~int64_t(15);
-    nst = static_cast<int>((bulk + chunk - 1) / chunk);
-    if (tid == 0) {
-      for (int s = 0; s < nst; ++s) mbar_init(&sm.bar[s], 1);
-      fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
-      const char* src = reinterpret_cast<const char*>(rc.g + rc.s0);
-      char* dst = reinterpret_cast<char*>(sl);
-      for (int s = 0; s < nst; ++s) {
-        const int64_t off = s * chunk;
-        const uint32_t sz = static_cast<uint32_t>((chunk < bulk - off ? chunk : bulk - off));
-        mbar_expect_tx(&sm.bar[s], sz);
-        bulk_copy_g2s(dst + off, src + off, sz, &sm.bar[s]);
-      }
-    }
-  }
-  // elements past the bulk part (unaligned rows, or a ragged tail) by plain loads
-  const int e_tail = static_cast<int>(bulk / static_cast<int64_t>(sizeof(E)));
-  for (int e = e_tail + tid; e < rc.L; e += kThreads) sl[e] = rc.g[rc.s0 + e];
-
-  for (int s = 0; s < nst; ++s) {
-    if (!mbar_wait_bounded(&sm.bar[s])) abort_ = 1;
-    const int v0 = static_cast<int>((s * chunk) / 16);
-    const int v1 = static_cast<int>((bulk < (s + 1) * chunk ? bulk : (s + 1) * chunk) / 16);
-    for (int v = v0 + tid; v < v1; v += kThreads) scan_vec(v);
-  }
-  __syncthreads();  // tail stores visible
-  for (int e = e_tail + tid; e < rc.L; e += kThreads) {
-    const float x = Fmt<E>::at(sl, e);
-    bad |= (x != x);
-    if (x > best) { best = x; best_idx = rc.s0 + e; }
-  }
-
-  // reduce (max value, lowest index), bad, abort
-  const int lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(FULL, best, o);
-    const int oi = __shfl_xor_sync(FULL, best_idx, o);
-    if (ov > best || (ov == best && oi < best_idx)) { best = ov; best_idx = oi; }
-    bad |= __shfl_xor_sync(FULL, bad, o);
-    abort_ |= __shfl_xor_sync(FULL, abort_, o);
-  }
-  if (lane == 0) { sm.wf[warp] = best; sm.wi[warp] = best_idx; sm.wi2[warp] = bad | (abort_ << 1); }
-  __syncthreads();
-  if (tid == 0) {
-    float bv = -INFINITY;
-    int bi = INT_MAX, fl = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      if (sm.wf[w] > bv || (sm.wf[w] == bv && sm.wi[w] < bi)) { bv = sm.wf[w]; bi = sm.wi[w]; }
-      fl |= sm.wi2[w];
-    }
-    Slot& s = C.mine(sm);
-    s.d[0] = ff(bv);
-    s.i[0] = bi;
-    s.i[1] = fl;
-  }
-  const Slot* mir = C.exchange(sm);
-  if (tid == 0) {
-    float bv = -INFINITY;
-    int bi = INT_MAX, fl = 0;
-    for (int r = 0; r < C.cs; ++r) {
-      const Slot* s = (&mir[r]);
-      const float v = s->d[0].hi;
-      const int i = s->i[0];
-      if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
-      fl |= s->i[1];
-    }
-    sm.m = bv;
-    sm.argmax = bi;
-    sm.bad = (fl & 1) || !(bv < INFINITY) || bi == INT_MAX;  // NaN, +inf, or no finite logit
-    sm.abort_ = (fl >> 1) & 1;
-  }
-  __syncthreads();
-}
-
-// ---- cluster-wide ordered total of weights over the resident row -------------
-// Leaves per-(rank, warp) totals in the mirror (d[1 + w] of each rank), for a
-// following cluster_ordered_draw with the same weights and no exchange between.
-template <typename E, typename WF>
-__device__ FF cluster_weight_total(const RowCtx<E>& rc, Scratch& sm, Cluster& C, WF wf) {
-  constexpr int N = Fmt<E>::N;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  auto wl = [&](float (&x)[N], int e0, int nvalid) {
-#pragma unroll
-    for (int j = 0; j < N; ++j) x[j] = (j < nvalid) ? wf(x[j], rc.s0 + e0 + j) : 0.0f;
-  };
-  const FF wt = warp_ordered_total<N>(rc.L, warp, lane, smem_loader(rc), wl);
-  if (lane == 0) sm.wtot[warp] = wt;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    Slot& s = C.mine(sm);
-    FF tot = ff(0.0f);
-    for (int w = 0; w < kWarps; ++w) {
-      s.d[1 + w] = sm.wtot[w];
-      tot = ff_add(tot, sm.wtot[w]);
-    }
-    s.d[0] = tot;
-  }
-  const Slot* mir = C.exchange(sm);
-  if (threadIdx.x == 0) {
-    FF z = ff(0.0f);
-    for (int r = 0; r < C.cs; ++r) z = ff_add(z, mir[r].d[0]);
-    sm.bd[0] = z;
-  }
-  __syncthreads();
-  const FF z = sm.bd[0];
-  __syncthreads();
-  return z;
-}
-
-// Ordered draw over the cluster-resident row with the weights of the preceding
-// cluster_weight_total (its totals still in the mirror).  The finding warp writes the token through
-// `emit(token)`.
-template <typename E, typename WF, typename Emit>
-__device__ void cluster_ordered_draw(const RowCtx<E>& rc, Scratch& sm, Cluster& C, double u, WF wf,
-                                     Emit emit) {
-  const Slot* mir = sm.mirror;
-  constexpr int N = Fmt<E>::N;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) {
-    FF total = ff(0.0f);
-    for (int r = 0; r < C.cs; ++r)
-      for (int w = 0; w < kWarps; ++w) total = ff_add(total, mir[r].d[1 + w]);
-    const FF target = ff_from_d(u * ff_to_d(total));
-    int fr = -1, fw = -1, lr = 0, lw = 0;
-    FF base = ff(0.0f), cum = ff(0.0f);
-    for (int r = 0; r < C.cs && fr < 0; ++r)
-      for (int w = 0; w < kWarps; ++w) {
-        const FF t = mir[r].d[1 + w];
-        if (t.hi > 0.0f) { lr = r; lw = w; }
-        const FF next = ff_add(cum, t);
-        if (ff_lt(target, next)) { fr = r; fw = w; base = cum; break; }
-        cum = next;
-      }
-    const int overflow = fr < 0;
-    if (overflow) { fr = lr; fw = lw; }
-    sm.bi[0] = fr;
-    sm.bi[1] = fw;
-    sm.bi[2] = overflow;
-    sm.bd[0] = target;
-    sm.bd[1] = base;
-  }
-  __syncthreads();
-  const int fr = sm.bi[0], fw = sm.bi[1];
-  const bool overflow = sm.bi[2] != 0;
-  const FF target = sm.bd[0], base = sm.bd[1];
-  __syncthreads();
-  if (C.rank == fr && warp == fw) {
-    auto wl = [&](float (&x)[N], int e0, int nvalid) {
-#pragma unroll
-      for (int j = 0; j < N; ++j) x[j] = (j < nvalid) ? wf(x[j], rc.s0 + e0 + j) : 0.0f;
-    };
-    const int e = warp_ordered_draw<N>(rc.L, warp, lane, smem_loader(rc), wl, target, base, overflow);
-    if (lane == 0) emit(e >= 0 ? rc.s0 + e : -1);
-  }
 }
 
 // ---- probe pass: counts / masses of elements >= each threshold ----------------
 // thr[0] > thr[1] > ... > thr[np-1]; restricted to `rcut` when `restricted`.
 // Cluster totals are returned in cnt_out / mass_out (all threads).
 template <typename E>
-__device__ void probe_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, const float (&thr)[kProbes], int np,
+__device__ void probe_pass(const RowCtx<E>& rc, Scratch& sm, Local& C, const float (&thr)[kProbes], int np,
                            bool with_mass, bool restricted, Cut rcut, int (&cnt_out)[kProbes],
                            FF (&mass_out)[kProbes]) {
   constexpr int N = Fmt<E>::N;
@@ -756,7 +703,7 @@ __device__ void probe_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, const f
 #pragma unroll
   for (int j = 0; j < kProbes; ++j) { cnt[j] = 0; mass[j] = 0.0f; }
   const float lowest = thr[np - 1];
-  for_warp_segment<N>(rc.L, warp, lane, smem_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
+  for_warp_segment<N>(rc.L, warp, lane, row_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
 #pragma unroll
     for (int j = 0; j < N; ++j) {
       if (j < nvalid && x[j] >= lowest) {
@@ -806,7 +753,7 @@ template <typename E, typename P>
 __device__ int warp_count(const RowCtx<E>& rc, int warp, int lane, P pred) {
   constexpr int N = Fmt<E>::N;
   int c = 0;
-  for_warp_segment<N>(rc.L, warp, lane, smem_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
+  for_warp_segment<N>(rc.L, warp, lane, row_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
 #pragma unroll
     for (int j = 0; j < N; ++j)
       if (j < nvalid && pred(x[j], rc.s0 + e0 + j)) ++c;
@@ -831,7 +778,7 @@ __device__ int cta_ordered_compact(const RowCtx<E>& rc, Scratch& sm, P pred, Emi
   }
   __syncthreads();
   int running = off;
-  for_warp_segment<N>(rc.L, warp, lane, smem_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
+  for_warp_segment<N>(rc.L, warp, lane, row_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
     int c = 0;
 #pragma unroll
     for (int j = 0; j < N; ++j)
@@ -848,21 +795,8 @@ __device__ int cta_ordered_compact(const RowCtx<E>& rc, Scratch& sm, P pred, Emi
 
 // ---- rank-0 helpers over the gathered candidate list -------------------------
 
-// Bitonic sort of skey[0..P) descending (P a power of two <= kCap).
-__device__ void bitonic_sort_desc(unsigned long long* skey, int P) {
-  for (int k = 2; k <= P; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < P; i += kThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long x = skey[i], y = skey[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? (x < y) : (x > y)) { skey[i] = y; skey[ixj] = x; }
-        }
-      }
-      __syncthreads();
-    }
-  }
+__device__ __forceinline__ unsigned long long sort_key(float v, int idx) {
+  return (static_cast<unsigned long long>(okey32(v)) << 32) | (0xffffffffu - static_cast<uint32_t>(idx));
 }
 __device__ __forceinline__ float skey_val(unsigned long long k) {
   return okey32_val(static_cast<uint32_t>(k >> 32));
@@ -877,11 +811,17 @@ __device__ __forceinline__ int skey_idx(unsigned long long k) {
 // if R == 0.
 template <typename WF>
 __device__ int list_ordered_draw(int n, double u, Scratch& sm, WF wf) {
-  const int i0 = 2 * threadIdx.x, i1 = i0 + 1;  // n <= kCap = 2 * kThreads
-  const float w0 = (i0 < n) ? wf(i0) : 0.0f;
-  const float w1 = (i1 < n) ? wf(i1) : 0.0f;
+  constexpr int G = kCap / kThreads;  // n <= kCap: G consecutive entries per thread
+  const int b0 = static_cast<int>(threadIdx.x) * G;
+  float w[G];
+  FF run = ff(0.0f);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    w[g] = (b0 + g < n) ? wf(b0 + g) : 0.0f;
+    run = ff_add(run, w[g]);
+  }
   FF total;
-  const FF excl = block_excl_scan_ff(ff_add(ff(w0), w1), &total, sm);
+  const FF excl = block_excl_scan_ff(run, &total, sm);
   if (threadIdx.x == 0) {
     sm.bi[0] = INT_MAX;
     sm.bi[1] = -1;
@@ -891,11 +831,18 @@ __device__ int list_ordered_draw(int n, double u, Scratch& sm, WF wf) {
   int r = -1;
   if (total.hi > 0.0f) {
     const FF target = sm.bd[0];
-    const FF c0 = ff_add(excl, w0), c1 = ff_add(c0, w1);
-    if (w0 > 0.0f && ff_lt(target, c0) && !ff_lt(target, excl)) atomicMin(&sm.bi[0], i0);
-    if (w1 > 0.0f && ff_lt(target, c1) && !ff_lt(target, c0)) atomicMin(&sm.bi[0], i1);
-    if (w1 > 0.0f) atomicMax(&sm.bi[1], i1);
-    else if (w0 > 0.0f) atomicMax(&sm.bi[1], i0);
+    FF c = excl;
+    int lastpos = -1;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const FF before = c;
+      c = ff_add(c, w[g]);
+      if (w[g] > 0.0f) {
+        lastpos = b0 + g;
+        if (ff_lt(target, c) && !ff_lt(target, before)) atomicMin(&sm.bi[0], b0 + g);
+      }
+    }
+    if (lastpos >= 0) atomicMax(&sm.bi[1], lastpos);
     __syncthreads();
     r = (sm.bi[0] != INT_MAX) ? sm.bi[0] : sm.bi[1];
   }
@@ -911,228 +858,27 @@ struct Bracket {
   FF mass_lo, mass_hi;
 };
 
-// ---- first pass ---------------------------------------------------------------
-// One sweep over the resident slice after the max is known.  It computes the
-// normaliser (when needed: no filter, or top-p without top-k), the counts and
-// masses of the elements above each of the first probe thresholds, and, per
-// warp, the index-ordered list of elements above the lowest threshold (up to
-// kWarpCap; more sets `overflow`).  One cluster exchange publishes everything.
-
-struct PassA {
-  FF z;
-  int cnt[kProbes];
-  FF mass[kProbes];
-  int overflow;
-};
-
-// First probe thresholds: m - W*scale on the data grid, strictly descending.
-template <typename E>
-__device__ int first_probes(float m, float scale, float (&thr)[kProbes]) {
-  const float W[kProbes] = {0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f, 8.f};
-  int np = 0;
-  uint32_t prev = Fmt<E>::key(m) + 1;
-  const uint32_t kmin = Fmt<E>::key(-INFINITY);
-  for (int j = 0; j < kProbes; ++j) {
-    const float t = Fmt<E>::round_to_grid(m - W[j] * scale);
-    if (!(t == t) || !(t > -INFINITY)) break;
-    uint32_t k = Fmt<E>::key(t);
-    if (k >= prev) k = prev - 1;
-    if (k <= kmin) break;
-    thr[np++] = Fmt<E>::val(k);
-    prev = k;
-  }
-  for (int j = np; j < kProbes; ++j) thr[j] = -INFINITY;
-  return np;
-}
-
-template <typename E>
-__device__ void first_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, bool need_z, bool filtered,
-                           bool with_mass, const float (&thr)[kProbes], int np, PassA& out) {
-  constexpr int N = Fmt<E>::N;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int cnt[kProbes];
-  float mass[kProbes];
-#pragma unroll
-  for (int p = 0; p < kProbes; ++p) { cnt[p] = 0; mass[p] = 0.0f; }
-  const float lowest = (filtered && np > 0) ? thr[np - 1] : INFINITY;
-  FF running = ff(0.0f);
-  int lcount = 0;  // warp-uniform list length
-  int32_t* widx = sm.cand_idx + warp * kWarpCap;
-  float* wval = sm.cand_val + warp * kWarpCap;
-  for_warp_segment<N>(rc.L, warp, lane, smem_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
-    if (need_z) {  // same arithmetic as warp_ordered_total with weights wexp
-      float s = 0.0f;
-#pragma unroll
-      for (int j = 0; j < N; ++j) s += (j < nvalid) ? wexp(x[j], rc.m, rc.c) : 0.0f;
-      running = ff_add(running, warp_sum_f(s));
-    }
-    int c = 0;
-#pragma unroll
-    for (int j = 0; j < N; ++j) c += (j < nvalid && x[j] >= lowest) ? 1 : 0;
-    if (__any_sync(FULL, c != 0)) {
-#pragma unroll
-      for (int j = 0; j < N; ++j) {
-        if (j < nvalid && x[j] >= lowest) {
-          const float w = with_mass ? wexp(x[j], rc.m, rc.c) : 0.0f;
-#pragma unroll
-          for (int p = 0; p < kProbes; ++p)
-            if (p < np && x[j] >= thr[p]) { cnt[p] += 1; mass[p] += w; }
-        }
-      }
-      const int incl = warp_incl_scan_i(c, lane);
-      int pos = lcount + incl - c;
-#pragma unroll
-      for (int j = 0; j < N; ++j) {
-        if (j < nvalid && x[j] >= lowest) {
-          if (pos < kWarpCap) { widx[pos] = rc.s0 + e0 + j; wval[pos] = x[j]; }
-          ++pos;
-        }
-      }
-      lcount += __shfl_sync(FULL, incl, 31);
-    }
-  });
-#pragma unroll
-  for (int p = 0; p < kProbes; ++p) {
-    cnt[p] = warp_sum_i(cnt[p]);
-    mass[p] = warp_sum_f(mass[p]);
-    if (lane == 0) { sm.pcnt[p][warp] = cnt[p]; sm.pmass[p][warp] = mass[p]; }
-  }
-  if (lane == 0) {
-    sm.wtot[warp] = running;
-    sm.wi2[warp] = min(lcount, kWarpCap);
-    sm.wi[warp] = lcount > kWarpCap;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    Slot& s = C.mine(sm);
-    FF z = ff(0.0f);
-    int of = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      s.d[1 + w] = sm.wtot[w];
-      z = ff_add(z, sm.wtot[w]);
-      of |= sm.wi[w];
-    }
-    s.d[0] = z;
-    for (int p = 0; p < kProbes; ++p) {
-      int ct = 0;
-      FF ms = ff(0.0f);
-      for (int w = 0; w < kWarps; ++w) { ct += sm.pcnt[p][w]; ms = ff_add(ms, sm.pmass[p][w]); }
-      s.i[p] = ct;
-      s.d[1 + kWarps + p] = ms;
-    }
-    s.i[kProbes] = of;
-  }
-  const Slot* mir = C.exchange(sm);
-  // thread 0 reduces the mirror in rank order; the whole CTA reads the result
-  if (threadIdx.x == 0) {
-    FF z = ff(0.0f);
-    int of = 0;
-    for (int r = 0; r < C.cs; ++r) { z = ff_add(z, mir[r].d[0]); of |= mir[r].i[kProbes]; }
-    for (int p = 0; p < kProbes; ++p) {
-      int ct = 0;
-      FF ms = ff(0.0f);
-      for (int r = 0; r < C.cs; ++r) { ct += mir[r].i[p]; ms = ff_add(ms, mir[r].d[1 + kWarps + p]); }
-      sm.bi[p] = ct;
-      sm.bd[p] = ms;
-    }
-    sm.bd[kProbes] = z;
-    sm.bi[kProbes] = of;
-  }
-  __syncthreads();
-  out.z = sm.bd[kProbes];
-  out.overflow = sm.bi[kProbes];
-  for (int p = 0; p < kProbes; ++p) { out.cnt[p] = sm.bi[p]; out.mass[p] = sm.bd[p]; }
-  __syncthreads();
-}
-
-// Bracket implied by the first pass's probes (same update rule as bracket_search).
-template <typename E>
-__device__ Bracket bracket_from_probes(float m, const float (&thr)[kProbes], int np, const PassA& pa,
-                                       bool mass_mode, int need_cnt, FF need_mass, int cnt_all,
-                                       FF mass_all, int* first_true_out) {
-  Bracket br;
-  br.lo = Fmt<E>::key(-INFINITY);
-  br.hi = Fmt<E>::key(m) + 1;
-  br.cnt_lo = cnt_all;
-  br.mass_lo = mass_all;
-  br.cnt_hi = 0;
-  br.mass_hi = ff(0.0f);
-  int ft = -1;
-  for (int j = 0; j < np; ++j) {  // thr[0] is the largest threshold
-    const bool ok = mass_mode ? !ff_lt(pa.mass[j], need_mass) : (pa.cnt[j] >= need_cnt);
-    if (ok) { ft = j; break; }
-  }
-  if (ft >= 0) {
-    br.lo = Fmt<E>::key(thr[ft]);
-    br.cnt_lo = pa.cnt[ft];
-    br.mass_lo = pa.mass[ft];
-    if (ft > 0) {
-      br.hi = Fmt<E>::key(thr[ft - 1]);
-      br.cnt_hi = pa.cnt[ft - 1];
-      br.mass_hi = pa.mass[ft - 1];
-    }
-  } else if (np > 0) {
-    br.hi = Fmt<E>::key(thr[np - 1]);
-    br.cnt_hi = pa.cnt[np - 1];
-    br.mass_hi = pa.mass[np - 1];
-  }
-  *first_true_out = ft;
-  return br;
-}
-
-// After a CTA has its candidates at cand_*[0 .. n) in index order: publish n,
-// and rank 0 appends the other ranks' lists after its own in one flat round of
-// remote loads.  Returns the cluster count on every CTA.
-__device__ int rank0_collect(Scratch& sm, Cluster& C, int n) {
-  if (threadIdx.x == 0) C.mine(sm).i[0] = n;
-  const Slot* mir = C.exchange(sm);
-  int off[kMaxCluster + 1];
-  off[0] = 0;
-  for (int r = 0; r < C.cs; ++r) off[r + 1] = off[r] + mir[r].i[0];
-  const int total = off[C.cs];
-  if (C.rank == 0) {
-    for (int j = n + threadIdx.x; j < min(total, kCap); j += kThreads) {
-      int r = 1;
-      while (r + 1 < C.cs && j >= off[r + 1]) ++r;
-      const int i = j - off[r];
-      sm.cand_idx[j] = C.cl.map_shared_rank(sm.cand_idx, r)[i];
-      sm.cand_val[j] = C.cl.map_shared_rank(sm.cand_val, r)[i];
-    }
-  }
-  __syncthreads();
-  return total;
-}
-
-// Candidates from the first pass's warp lists: keep entries >= lo_val, compact
-// them (warp order = index order) to the front, and collect them on rank 0.
-__device__ int lists_gather(Scratch& sm, Cluster& C, float lo_val) {
-  const int j0 = 2 * threadIdx.x, j1 = j0 + 1;  // 2 * kThreads == kCap slots
-  const int f0 = (j0 % kWarpCap) < sm.wi2[j0 / kWarpCap] && sm.cand_val[j0] >= lo_val;
-  const int f1 = (j1 % kWarpCap) < sm.wi2[j1 / kWarpCap] && sm.cand_val[j1] >= lo_val;
-  const int32_t i0 = sm.cand_idx[j0], i1 = sm.cand_idx[j1];
-  const float v0 = sm.cand_val[j0], v1 = sm.cand_val[j1];
-  int tot;
-  const int pos = block_excl_scan_i(f0 + f1, &tot, sm);
-  if (f0) { sm.cand_idx[pos] = i0; sm.cand_val[pos] = v0; }
-  if (f1) { sm.cand_idx[pos + f0] = i1; sm.cand_val[pos + f0] = v1; }
-  __syncthreads();
-  return rank0_collect(sm, C, tot);
+// The CTA's candidates sit at cand_*[0 .. n) in index order; make them visible
+// to the whole CTA and return n.
+__device__ int rank0_collect(Scratch& sm, Local& C, int n) {
+  C.exchange(sm);
+  return n;
 }
 
 // ---- exact cut ----------------------------------------------------------------
 
 
-// Narrow `br` until cnt_lo <= kCap (sortable on chip) or hi == lo + 1 (one key
+// Narrow `br` until cnt_lo <= cap (sortable on chip) or hi == lo + 1 (one key
 // value).  pred = (mass_mode ? mass >= need_mass : count >= need_cnt).  Unless
 // `probed` (a first pass already probed near the max), the first probes sit at
 // m - W*scale; later ones split [lo, hi) evenly in key space.
 template <typename E>
-__device__ Bracket bracket_search(const RowCtx<E>& rc, Scratch& sm, Cluster& C, bool mass_mode, int need_cnt,
+__device__ Bracket bracket_search(const RowCtx<E>& rc, Scratch& sm, Local& C, bool mass_mode, int need_cnt,
                                   FF need_mass, float scale, bool restricted, Cut rcut, Bracket br,
-                                  bool probed) {
+                                  bool probed, int cap) {
   const float W[kProbes] = {0.5f, 1.f, 2.f, 3.f, 4.f, 6.f, 8.f, 16.f};
   for (int pass = probed ? 1 : 0; pass < kMaxPasses; ++pass) {
-    if (br.cnt_lo <= kCap || br.hi - br.lo <= 1) break;
+    if (br.cnt_lo <= cap || br.hi - br.lo <= 1) break;
     uint32_t keys[kProbes];  // ascending, strictly inside (lo, hi)
     int np = 0;
     const uint32_t span = br.hi - br.lo - 1;
@@ -1189,7 +935,7 @@ __device__ Bracket bracket_search(const RowCtx<E>& rc, Scratch& sm, Cluster& C, 
 // Gather every element >= lo_val (and kept by rcut) into rank 0's candidate
 // list, in index order; returns the cluster count on every CTA.
 template <typename E>
-__device__ int gather_candidates(const RowCtx<E>& rc, Scratch& sm, Cluster& C, float lo_val, bool restricted,
+__device__ int gather_candidates(const RowCtx<E>& rc, Scratch& sm, Local& C, float lo_val, bool restricted,
                                  Cut rcut) {
   auto pred = [&](float l, int x) { return l >= lo_val && (!restricted || rcut.keep(l, x)); };
   const int n = cta_ordered_compact<E>(rc, sm, pred, [&](int pos, float l, int x) {
@@ -1198,58 +944,108 @@ __device__ int gather_candidates(const RowCtx<E>& rc, Scratch& sm, Cluster& C, f
   return rank0_collect(sm, C, n);
 }
 
-// Rank 0 (all its threads): sort the n gathered candidates by (logit desc, index
-// asc), keep the first need_k (need_k > 0), then the shortest prefix whose mass
-// reaches top_p * Z (Z = the kept top-k mass, or z_for_p without top-k).
-// Leaves Z_f in sm.bd[0], the cut value in sm.bd[1], the kept count in sm.bi[0],
-// the cut index in sm.bi[1] and the gathered count in sm.bi[7].
-template <typename E>
-__device__ void rank0_sort_and_cut(const RowCtx<E>& rc, Scratch& sm, SortBuf sb, int n, int need_k, float top_p,
-                                   FF z_for_p) {
-  unsigned long long* skey = sb.skey;
-  FF* scan = sb.scan;
-  int P = 1;
-  while (P < n) P <<= 1;
-  for (int i = threadIdx.x; i < P; i += kThreads)
-    skey[i] = (i < n) ? ((static_cast<unsigned long long>(okey32(sm.cand_val[i])) << 32) |
-                            (0xffffffffu - static_cast<uint32_t>(sm.cand_idx[i])))
-                         : 0ull;
-  __syncthreads();
-  bitonic_sort_desc(skey, P);
-  const int nk = (need_k > 0) ? min(need_k, n) : n;
-  const int i0 = 2 * threadIdx.x, i1 = i0 + 1;
-  const float w0 = (i0 < nk) ? wexp(skey_val(skey[i0]), rc.m, rc.c) : 0.0f;
-  const float w1 = (i1 < nk) ? wexp(skey_val(skey[i1]), rc.m, rc.c) : 0.0f;
+// The whole CTA: sort n candidates (idx[], val[], index order) by (logit desc,
+// index asc), keep the first need_k (need_k > 0), then the shortest prefix whose
+// mass reaches top_p * Z (Z = the kept top-k mass, or z_for_p without top-k).
+// Weights are 2^((l - m) c).  Returns in out: the cut (value, index), the kept
+// count, Z_f (mass of the kept prefix), the mass of the whole sorted list, and
+// whether the top-p crossing was reached within the list.
+struct CutResult {
+  float tv;
+  int ti;
+  int nkeep;
+  FF zf;
   FF total;
-  const FF excl = block_excl_scan_ff(ff_add(ff(w0), w1), &total, sm);
-  if (i0 < nk) scan[i0] = ff_add(excl, w0);
-  if (i1 < nk) scan[i1] = ff_add(ff_add(excl, w0), w1);
+  int reached;
+};
+
+__device__ CutResult sort_and_cut(float m, float c, const int32_t* idx, const float* val, int n, SortBuf sb,
+                                  int need_k, float top_p, FF z_for_p, Scratch& sm) {
+  constexpr int GMAX = kPool / kThreads;
+  unsigned long long* skey = sb.skey;
+  // sort in registers (zero keys pad, and sort last), then lay the keys out
+  // in order for the prefix and the cut
+  if (n <= 2 * kThreads) {
+    unsigned long long key[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = threadIdx.x * 2 + r;
+      key[r] = (i < n) ? sort_key(val[i], idx[i]) : 0ull;
+    }
+    block_sort_keys_desc<2>(key, skey);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) skey[threadIdx.x * 2 + r] = key[r];
+  } else {
+    unsigned long long key[kPool / kThreads];
+#pragma unroll
+    for (int r = 0; r < kPool / kThreads; ++r) {
+      const int i = threadIdx.x * (kPool / kThreads) + r;
+      key[r] = (i < n) ? sort_key(val[i], idx[i]) : 0ull;
+    }
+    block_sort_keys_desc<kPool / kThreads>(key, skey);
+#pragma unroll
+    for (int r = 0; r < kPool / kThreads; ++r) skey[threadIdx.x * (kPool / kThreads) + r] = key[r];
+  }
+  __syncthreads();
+  const int nk = (need_k > 0) ? min(need_k, n) : n;
+  // inclusive prefix of the weights in sorted order: G consecutive entries per
+  // thread, kept in registers
+  const int G = max(1, (nk + kThreads - 1) / kThreads);
+  const int b0 = threadIdx.x * G;
+  FF pre[GMAX];
+  FF run = ff(0.0f);
+#pragma unroll
+  for (int g = 0; g < GMAX; ++g) {
+    const int i = b0 + g;
+    if (g < G && i < nk) run = ff_add(run, wexp(skey_val(skey[i]), m, c));
+    pre[g] = run;
+  }
+  FF total;
+  const FF excl = block_excl_scan_ff(run, &total, sm);
   if (threadIdx.x == 0) sm.bi[2] = INT_MAX;
   __syncthreads();
   int cut = nk - 1;
+  int reached = 1;
   if (top_p < 1.0f) {
     const FF zk = (need_k > 0) ? total : z_for_p;
     const FF need = ff_mul(zk, top_p);
-    if (i0 < nk && !ff_lt(scan[i0], need)) atomicMin(&sm.bi[2], i0);
-    if (i1 < nk && !ff_lt(scan[i1], need)) atomicMin(&sm.bi[2], i1);
+    bool hit = false;
+#pragma unroll
+    for (int g = 0; g < GMAX; ++g) {
+      const int i = b0 + g;
+      if (!hit && g < G && i < nk && !ff_lt(ff_add(excl, pre[g]), need)) {
+        atomicMin(&sm.bi[2], i);
+        hit = true;
+      }
+    }
     __syncthreads();
-    if (sm.bi[2] != INT_MAX) cut = sm.bi[2];  // otherwise rounding: keep all nk
+    if (sm.bi[2] != INT_MAX) cut = sm.bi[2];
+    else reached = 0;  // the list's mass stays below top_p * Z
+  }
+  // Z_f = the prefix at the cut, published by the thread that holds it
+  if (threadIdx.x == cut / G) {
+    FF z = ff(0.0f);
+#pragma unroll
+    for (int g = 0; g < GMAX; ++g)
+      if (g == cut - b0) z = ff_add(excl, pre[g]);
+    sm.bd[2] = z;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    sm.bd[0] = scan[cut];
-    sm.bd[1] = ff(skey_val(skey[cut]));
-    sm.bi[0] = cut + 1;
-    sm.bi[1] = skey_idx(skey[cut]);
-    sm.bi[7] = n;  // gathered count (the kept list is filtered from these)
-  }
+  CutResult r;
+  r.tv = skey_val(skey[cut]);
+  r.ti = skey_idx(skey[cut]);
+  r.nkeep = cut + 1;
+  r.zf = sm.bd[2];
+  r.total = total;
+  r.reached = reached;
   __syncthreads();
+  return r;
 }
 
 // Tie cut: index of the c-th (1-based) element equal to tie_val (and kept by
 // rcut), in index order across the cluster.  Same value on every CTA.
 template <typename E>
-__device__ int tie_locate(const RowCtx<E>& rc, Scratch& sm, Cluster& C, float tie_val, int c, bool restricted,
+__device__ int tie_locate(const RowCtx<E>& rc, Scratch& sm, Local& C, float tie_val, int c, bool restricted,
                           Cut rcut) {
   constexpr int N = Fmt<E>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1279,7 +1075,7 @@ __device__ int tie_locate(const RowCtx<E>& rc, Scratch& sm, Cluster& C, float ti
   __syncthreads();
   if (C.rank == fr && warp == fw) {
     int running = 0, found = -1;
-    for_warp_segment<N>(rc.L, warp, lane, smem_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
+    for_warp_segment<N>(rc.L, warp, lane, row_loader(rc), [&](float (&x)[N], int e0, int nvalid) {
       int cnt = 0;
 #pragma unroll
       for (int j = 0; j < N; ++j)
@@ -1310,7 +1106,7 @@ __device__ int tie_locate(const RowCtx<E>& rc, Scratch& sm, Cluster& C, float ti
 // with write_list and a kept set that fits kCap, the kept set is written in index
 // order to lidx / lw.
 template <typename E>
-__device__ void kept_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, Cut cut, bool write_list, int32_t* lidx,
+__device__ void kept_pass(const RowCtx<E>& rc, Scratch& sm, Local& C, Cut cut, bool write_list, int32_t* lidx,
                           float* lw, int* nkeep, FF* zf, int* list_len) {
   constexpr int N = Fmt<E>::N;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1320,7 +1116,7 @@ __device__ void kept_pass(const RowCtx<E>& rc, Scratch& sm, Cluster& C, Cut cut,
     for (int j = 0; j < N; ++j)
       x[j] = (j < nvalid && cut.keep(x[j], rc.s0 + e0 + j)) ? wexp(x[j], rc.m, rc.c) : 0.0f;
   };
-  const FF wt = warp_ordered_total<N>(rc.L, warp, lane, smem_loader(rc), wl);
+  const FF wt = warp_ordered_total<N>(rc.L, warp, lane, row_loader(rc), wl);
   const int wc = warp_count<E>(rc, warp, lane, pred);
   if (lane == 0) { sm.wtot[warp] = wt; sm.wi2[warp] = wc; }
   __syncthreads();
@@ -1373,7 +1169,6 @@ __device__ RowInfo decode_job(const KArgs& a, int job) {
     ri.t = ri.is_target ? r : r - (a.K + 1);
     ri.row_off = ri.is_target ? static_cast<int64_t>(ri.b) * a.tgt_seq + static_cast<int64_t>(ri.t) * a.tgt_row
                               : static_cast<int64_t>(ri.b) * a.drf_seq + static_cast<int64_t>(ri.t) * a.drf_row;
-    if (ri.t < a.K) ri.tok = a.tokens[static_cast<int64_t>(ri.b) * a.K + ri.t];
   } else {
     ri.b = job / a.K;
     ri.t = job % a.K;
@@ -1574,233 +1369,758 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
   }
 }
 
+
 // ---------------------------------------------------------------------------
-// the kernel: one cluster per row
+// row merge, run by the CTA that finishes a row's last chunk
 
 template <typename E>
-__global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
-  Cluster C;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
-  E* sl = reinterpret_cast<E*>(smem_raw + sizeof(Scratch));
-  const SortBuf sb{reinterpret_cast<unsigned long long*>(sl),
-                   reinterpret_cast<FF*>(reinterpret_cast<unsigned char*>(sl) + kCap * sizeof(unsigned long long))};
-  const int tid = threadIdx.x;
-  const int job = static_cast<int>(blockIdx.x) / C.cs;
-  const RowInfo ri = decode_job(a, job);
-
-  RowCtx<E> rc;
-  rc.g = static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off;
-  rc.sl = sl;
-  rc.s0 = C.rank * a.S;
-  rc.L = min(a.S, a.V - rc.s0);
-  rc.c = a.c;
-  rc.m = 0.0f;
-
-  load_and_scan<E>(a, rc, sl, sm, C);
-  rc.m = sm.m;
-  const bool abort_ = sm.abort_ != 0;
-  const bool bad = (sm.bad != 0) || abort_;
-  const int argmax = sm.argmax;
-
-  spec_row_stat* rec = a.rows + job;
-  int32_t* lidx = a.list_idx + static_cast<int64_t>(job) * kCap;
-  float* lw = a.list_w + static_cast<int64_t>(job) * kCap;
+__device__ void general_cut(const KArgs& a, const RowCtx<E>& rg, Scratch& sm, Local& C, SortBuf sb, FF z,
+                            Cut* cut_out, FF* zf_out, int* list_len_out, int32_t* lidx, float* lw) {
+  // exact selection over the whole row in global memory (rg.gsrc): top-k by count,
+  // then top-p by mass within it; ends in an on-chip sort or a tie cut by index
   const bool use_k = a.top_k > 0 && a.top_k < a.V;
   const bool use_p = a.top_p < 1.0f;
+  Cut cut = cut_all();
+  FF zf = z, zk = z;
+  int list_len = -1;
+  bool sorted = false, restricted = false, final_tie = false;
+  Cut kcut = cut_all();
+  CutResult res;
+  int gathered = 0;
+  auto fresh = [&](int cnt_all, FF mass_all) {
+    Bracket br;
+    br.lo = Fmt<E>::key(-INFINITY);
+    br.hi = Fmt<E>::key(rg.m) + 1;
+    br.cnt_lo = cnt_all;
+    br.mass_lo = mass_all;
+    br.cnt_hi = 0;
+    br.mass_hi = ff(0.0f);
+    return br;
+  };
+  if (use_k) {
+    Bracket br = bracket_search<E>(rg, sm, C, false, a.top_k, ff(0.0f), 1.0f, false, cut_all(),
+                                   fresh(a.V, ff(0.0f)), false, kCap);
+    if (br.cnt_lo <= kCap) {
+      gathered = gather_candidates<E>(rg, sm, C, Fmt<E>::val(br.lo), false, cut_all());
+      res = sort_and_cut(rg.m, rg.c, sm.cand_idx, sm.cand_val, gathered, sb, a.top_k, use_p ? a.top_p : 1.0f,
+                         ff(0.0f), sm);
+      sorted = true;
+    } else {
+      const float tv = Fmt<E>::val(br.lo);
+      kcut = Cut{tv, tie_locate<E>(rg, sm, C, tv, a.top_k - br.cnt_hi, false, cut_all())};
+      restricted = true;
+      if (!use_p) { cut = kcut; final_tie = true; }
+    }
+  }
+  if (use_p && !sorted) {
+    int cnt_all = a.V;
+    if (restricted) {
+      int ll;
+      kept_pass<E>(rg, sm, C, kcut, false, nullptr, nullptr, &cnt_all, &zk, &ll);
+    }
+    const FF need = ff_mul(zk, a.top_p);
+    const Bracket br = bracket_search<E>(rg, sm, C, true, 0, need, a.temp, restricted, kcut,
+                                         fresh(cnt_all, zk), false, kCap);
+    if (br.cnt_lo <= kCap) {
+      gathered = gather_candidates<E>(rg, sm, C, Fmt<E>::val(br.lo), restricted, kcut);
+      res = sort_and_cut(rg.m, rg.c, sm.cand_idx, sm.cand_val, gathered, sb, 0, a.top_p, zk, sm);
+      sorted = true;
+    } else {
+      const float tv = Fmt<E>::val(br.lo);
+      const float w = wexp(tv, rg.m, rg.c);
+      const int ties = br.cnt_lo - br.cnt_hi;
+      int c = ties;
+      if (w > 0.0f) {  // smallest c with mass_hi + c * w >= need
+        const FF rem = ff_sub(need, br.mass_hi);
+        const float k = ceilf((rem.hi + rem.lo) / w);
+        c = static_cast<int>(fminf(fmaxf(k, 1.0f), static_cast<float>(ties)));
+      }
+      cut = Cut{tv, tie_locate<E>(rg, sm, C, tv, c, restricted, kcut)};
+      final_tie = true;
+    }
+  }
+  if (sorted) {
+    cut = Cut{res.tv, res.ti};
+    zf = res.zf;
+    // the kept list = the gathered candidates (index order) kept by the cut
+    if (res.nkeep <= kCap) {
+      constexpr int G = kCap / kThreads;  // gathered <= kCap: G consecutive entries per thread
+      const int b0 = static_cast<int>(threadIdx.x) * G;
+      int cnt = 0;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        if (b0 + g < gathered && cut.keep(sm.cand_val[b0 + g], sm.cand_idx[b0 + g])) ++cnt;
+      int tot;
+      int pos = block_excl_scan_i(cnt, &tot, sm);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int i = b0 + g;
+        if (i < gathered && cut.keep(sm.cand_val[i], sm.cand_idx[i])) {
+          lidx[pos] = sm.cand_idx[i];
+          lw[pos] = wexp(sm.cand_val[i], rg.m, rg.c);
+          ++pos;
+        }
+      }
+      list_len = tot;
+      __syncthreads();
+    }
+  }
+  if (final_tie) {
+    int nk;
+    kept_pass<E>(rg, sm, C, cut, true, lidx, lw, &nk, &zf, &list_len);
+  }
+  *cut_out = cut;
+  *zf_out = zf;
+  *list_len_out = list_len;
+}
+
+// Top-k streaming floor: sort the pool's keys (in a free ring slot), take the k-th
+// candidate (value, index) as the floor theta, and keep exactly the pool entries
+// at or above it, in their (index) order.  Later chunks only need elements above
+// theta's value: their ties at that value have larger indices.
+// ---------------------------------------------------------------------------
+// row merge, run by the CTA that finishes a row's last segment
+
+// Kept set (the sorted prefix skey[0, n)) written in index order: each entry's
+// position is the number of kept entries with a smaller index.
+__device__ void write_kept_by_index(const unsigned long long* skey, int n, float m, float c, int32_t* lidx,
+                                    float* lw, Scratch& sm) {
+  int32_t* kidx = sm.cand_idx;  // the indices, unpacked once
+  for (int i = threadIdx.x; i < n; i += kThreads) kidx[i] = skey_idx(skey[i]);
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const int xi = kidx[i];
+    int pos = 0;
+    for (int j = 0; j < n; ++j) pos += (kidx[j] < xi) ? 1 : 0;
+    lidx[pos] = xi;
+    lw[pos] = wexp(skey_val(skey[i]), m, c);
+  }
+  __syncthreads();
+}
+
+// Fold the row's segment records into sm.row_*: max, first argmax, normaliser
+// (each segment's sum rescaled to the row max, float-float, fixed order),
+// flags, the largest theta and per-segment k-th value; then gather the
+// segments' lists into the pool.  Records are staged a tile at a time in the
+// sort-key buffer and folded by warp 0, 32 at a time.
+__device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int32_t* pidx, float* pval) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  SegRec* stage = reinterpret_cast<SegRec*>(sb.skey);
+  const SegRec* recs = a.segs + static_cast<int64_t>(row) * a.nseg;
+  const int ns = a.nseg;
+  float m = -INFINITY, th = -INFINITY, kl = -INFINITY;
+  int am = -1, fl = 0, total = 0;
+  FF z = ff(0.0f);
+  for (int t0 = 0; t0 < ns; t0 += kThreads) {
+    const int nt = min(kThreads, ns - t0);
+    __syncthreads();
+    if (tid < nt) {
+      const int4* src = reinterpret_cast<const int4*>(recs + t0 + tid);
+      int4* dst = reinterpret_cast<int4*>(stage + tid);
+#pragma unroll
+      for (int w = 0; w < static_cast<int>(sizeof(SegRec) / 16); ++w) dst[w] = __ldcg(src + w);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      for (int c0 = 0; c0 < nt; c0 += 32) {
+        const int s = c0 + lane;
+        const bool valid = s < nt;
+        const int flags = valid ? stage[s].flags : 0;
+        const bool good = valid && !(flags & kSegBad);
+        const float ms = good ? stage[s].m : -INFINITY;
+        const int nc = valid ? stage[s].ncand : 0;
+        const int incl = warp_incl_scan_i(nc, lane);
+        if (valid) stage[s].off = total + incl - nc;
+        total += __shfl_sync(FULL, incl, 31);
+        fl |= static_cast<int>(__reduce_or_sync(FULL, static_cast<unsigned>(flags)));
+        float cm = ms;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, o));
+        if (cm > m) {  // a new row max (uniform): rescale the sum so far
+          if (z.hi > 0.0f) z = ff_mul(z, exp2f((m - cm) * a.c));
+          m = cm;
+          const unsigned hit = __ballot_sync(FULL, good && ms == cm);
+          am = __shfl_sync(FULL, valid ? stage[s].argmax : -1, __ffs(hit) - 1);
+        }
+        FF zs = ff(0.0f);
+        if (good && stage[s].z_hi > 0.0f) zs = ff_mul(FF{stage[s].z_hi, stage[s].z_lo}, exp2f((ms - m) * a.c));
+        z = ff_add(z, warp_sum_ff(zs));
+        float tv = good ? stage[s].theta : -INFINITY, kv = good ? stage[s].kth : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          tv = fmaxf(tv, __shfl_xor_sync(FULL, tv, o));
+          kv = fmaxf(kv, __shfl_xor_sync(FULL, kv, o));
+        }
+        th = fmaxf(th, tv);
+        kl = fmaxf(kl, kv);
+      }
+    }
+  }
+  if (tid == 0) {
+    sm.row_m = m;
+    sm.row_argmax = am;
+    sm.row_flags = fl;
+    sm.row_theta = th;
+    sm.row_kth = kl;
+    sm.row_z = z;
+    // the pool's segment offsets are staged for one tile only
+    sm.row_over = (ns > kThreads) || (fl & kSegOver) || (a.top_k <= 0 && total > kPool);
+    sm.pool_n = total;
+    sm.seg_n = 0;
+  }
+  __syncthreads();
+  // Gather the pool.  Top-k keeps only entries >= the largest per-segment k-th
+  // value: the row's k-th largest is at least that, so no entry below it can
+  // be kept.  Entry e of the concatenated lists belongs to the last segment
+  // whose offset is <= e.  Each thread issues up to eight loads at once.
+  total = sm.pool_n;  // folded by warp 0
+  if (a.filt && !sm.row_over && !(sm.row_flags & kSegBad) && total <= kListTable) {
+    const uint2* cand = a.seg_cand + static_cast<int64_t>(row) * a.nseg * kSegCap;
+    const float floor_v = (a.top_k > 0) ? sm.row_kth : -INFINITY;
+    // entry -> segment table (one byte per entry; ns <= kThreads <= 255)
+    uint8_t* segof = reinterpret_cast<uint8_t*>(sb.skey + kPool);
+    for (int s = tid; s < ns; s += kThreads)
+      for (int i = 0; i < stage[s].ncand; ++i) segof[stage[s].off + i] = static_cast<uint8_t>(s);
+    __syncthreads();
+    constexpr int U = 8;
+    for (int base = 0; base < total; base += kThreads * U) {
+      uint2 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = base + u * kThreads + tid;
+        v[u] = make_uint2(0u, 0xff800000u);  // -inf: never kept
+        if (e < total) {
+          const int s = segof[e];
+          v[u] = __ldcg(cand + static_cast<int64_t>(s) * kSegCap + (e - stage[s].off));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float x = __uint_as_float(v[u].y);
+        if (x > -INFINITY && x >= floor_v) {
+          const int pos = atomicAdd(&sm.seg_n, 1);
+          if (pos < kPool) {
+            pidx[pos] = static_cast<int32_t>(v[u].x);
+            pval[pos] = x;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      sm.pool_n = sm.seg_n;
+      if (sm.seg_n > kPool) sm.row_over = 1;
+    }
+  } else if (a.filt && tid == 0) {
+    sm.row_over = 1;  // more listed entries than the table holds
+  }
+  __syncthreads();
+}
+
+// Row end: exact cut from the pool (or the general path), record, draw.
+template <typename E>
+__device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scratch& sm, Local& C, SortBuf sb,
+                           const int32_t* pool_idx, const float* pool_val) {
+  const int tid = threadIdx.x;
+  const float m = sm.row_m;
+  const int argmax = sm.row_argmax;
+  const int fl = sm.row_flags;
+  // NaN / +inf in a segment, or no finite value in the row
+  const bool bad = (fl & kSegBad) || !(m > -INFINITY);
+  const FF z = sm.row_z;
+  const bool over = sm.row_over != 0;
+  const int total = sm.pool_n;
+  const float theta = sm.row_theta;
+  __syncthreads();
+
+  spec_row_stat* rec = a.rows + ri.job;
+  int32_t* lidx = a.list_idx + static_cast<int64_t>(ri.job) * kCap;
+  float* lw = a.list_w + static_cast<int64_t>(ri.job) * kCap;
+  const bool use_k = a.top_k > 0 && a.top_k < a.V;
+  const bool use_p = a.top_p < 1.0f;
+  RowCtx<E> rg;
+  rg.g = grow;
+  rg.sl = grow;
+  rg.s0 = 0;
+  rg.L = a.V;
+  rg.m = m;
+  rg.c = a.c;
+  rg.gsrc = 1;
+  rg.aligned = a.aligned;
 
   Cut cut = cut_all();
-  FF zf = ff(1.0f);
+  FF zf = z;
   int list_len = -1;
-  bool rank0_list = false;  // kept list sits in rank 0's candidate arrays
-
-  if (!bad && !a.greedy) {
-    // first pass: normaliser (no filter, or top-p without top-k), first probes and
-    // candidate lists (top-k by count, else top-p by mass)
-    const bool need_z = !use_k;
-    const bool filtered = use_k || use_p;
-    const bool mass_mode = !use_k;
-    float thr[kProbes];
-    const int np = filtered ? first_probes<E>(rc.m, use_k ? 1.0f : a.temp, thr) : 0;
-    PassA pa;
-    first_pass<E>(rc, sm, C, need_z, filtered, filtered && mass_mode, thr, np, pa);
-    if (!filtered) {
-      zf = pa.z;
-    } else {
-      FF zk = pa.z;
-      bool restricted = false, final_tie = false;
-      Cut kcut = cut_all();
-      if (use_k) {
-        // stage A: top-k by count
-        int ft;
-        Bracket br = bracket_from_probes<E>(rc.m, thr, np, pa, false, a.top_k, ff(0.0f), a.V, ff(0.0f), &ft);
-        int n = -1;
-        if (ft >= 0 && br.cnt_lo <= kCap && !pa.overflow) {
-          n = lists_gather(sm, C, Fmt<E>::val(br.lo));
-        } else {
-          br = bracket_search<E>(rc, sm, C, false, a.top_k, ff(0.0f), 1.0f, false, cut_all(), br, np > 0);
-          if (br.cnt_lo <= kCap) n = gather_candidates<E>(rc, sm, C, Fmt<E>::val(br.lo), false, cut_all());
+  if (!bad && !a.greedy && (use_k || use_p)) {
+    bool done = false;
+    if (!over && total > 0) {
+      const CutResult res = sort_and_cut(m, a.c, pool_idx, pool_val, total, sb, use_k ? a.top_k : 0,
+                                         use_p ? a.top_p : 1.0f, z, sm);
+      // exact when the pool holds the row's top-k, or when the top-p prefix
+      // closes at or above every segment's candidate floor
+      if (use_k || (res.reached && theta <= res.tv)) {
+        cut = Cut{res.tv, res.ti};
+        zf = res.zf;
+        if (res.nkeep <= kCap) {
+          write_kept_by_index(sb.skey, res.nkeep, m, a.c, lidx, lw, sm);
+          list_len = res.nkeep;
         }
-        if (n >= 0) {
-          if (C.rank == 0) rank0_sort_and_cut<E>(rc, sm, sb, n, a.top_k, use_p ? a.top_p : 1.0f, ff(0.0f));
-          rank0_list = true;
-        } else {
-          const float tv = Fmt<E>::val(br.lo);
-          const int ti = tie_locate<E>(rc, sm, C, tv, a.top_k - br.cnt_hi, false, cut_all());
-          kcut = Cut{tv, ti};
-          restricted = true;
-          if (!use_p) { cut = kcut; final_tie = true; }
-        }
+        done = true;
       }
-      if (use_p && !rank0_list) {
-        // stage B: top-p by mass, within the top-k set when stage A ended in a tie cut
-        Bracket br;
-        int ft = -1;
-        if (restricted) {
-          int nk, ll;
-          kept_pass<E>(rc, sm, C, kcut, false, nullptr, nullptr, &nk, &zk, &ll);
-          br.lo = Fmt<E>::key(-INFINITY);
-          br.hi = Fmt<E>::key(rc.m) + 1;
-          br.cnt_lo = nk;
-          br.mass_lo = zk;
-          br.cnt_hi = 0;
-          br.mass_hi = ff(0.0f);
-        } else {
-          br = bracket_from_probes<E>(rc.m, thr, np, pa, true, 0, ff_mul(zk, a.top_p), a.V, zk, &ft);
-        }
-        const FF need = ff_mul(zk, a.top_p);
-        int n = -1;
-        if (!restricted && ft >= 0 && br.cnt_lo <= kCap && !pa.overflow) {
-          n = lists_gather(sm, C, Fmt<E>::val(br.lo));
-        } else {
-          br = bracket_search<E>(rc, sm, C, true, 0, need, a.temp, restricted, kcut, br, !restricted && np > 0);
-          if (br.cnt_lo <= kCap) n = gather_candidates<E>(rc, sm, C, Fmt<E>::val(br.lo), restricted, kcut);
-        }
-        if (n >= 0) {
-          if (C.rank == 0) rank0_sort_and_cut<E>(rc, sm, sb, n, 0, a.top_p, zk);
-          rank0_list = true;
-        } else {
-          const float tv = Fmt<E>::val(br.lo);
-          const float w = wexp(tv, rc.m, rc.c);
-          const int ties = br.cnt_lo - br.cnt_hi;
-          int c = ties;
-          if (w > 0.0f) {  // smallest c with mass_hi + c * w >= need
-            const FF rem = ff_sub(need, br.mass_hi);
-            const float k = ceilf((rem.hi + rem.lo) / w);
-            c = static_cast<int>(fminf(fmaxf(k, 1.0f), static_cast<float>(ties)));
-          }
-          const int ti = tie_locate<E>(rc, sm, C, tv, c, restricted, kcut);
-          cut = Cut{tv, ti};
-          final_tie = true;
-        }
-      }
-      if (final_tie) {
-        int nk;
-        kept_pass<E>(rc, sm, C, cut, true, lidx, lw, &nk, &zf, &list_len);
-      }
+      __syncthreads();
     }
+    if (!done) general_cut<E>(a, rg, sm, C, sb, z, &cut, &zf, &list_len, lidx, lw);
   }
 
-  // rank 0: the kept list = gathered candidates (index order) kept by the cut
-  if (rank0_list && C.rank == 0) {
-    cut = Cut{sm.bd[1].hi, sm.bi[1]};
-    zf = sm.bd[0];
-    list_len = sm.bi[0];
-    const int gathered = sm.bi[7];
-    const int i0 = 2 * tid, i1 = i0 + 1;
-    const int f0 = (i0 < gathered) && cut.keep(sm.cand_val[i0], sm.cand_idx[i0]);
-    const int f1 = (i1 < gathered) && cut.keep(sm.cand_val[i1], sm.cand_idx[i1]);
-    int tot;
-    const int pos = block_excl_scan_i(f0 + f1, &tot, sm);
-    if (f0) { lidx[pos] = sm.cand_idx[i0]; lw[pos] = wexp(sm.cand_val[i0], rc.m, rc.c); }
-    if (f1) { lidx[pos + f0] = sm.cand_idx[i1]; lw[pos + f0] = wexp(sm.cand_val[i1], rc.m, rc.c); }
-    __syncthreads();
-  }
-
-  // sample mode: draw the token of this row
+  // sample mode: draw this row's token
   if (a.mode == kModeSample) {
     const double u = a.greedy ? 0.0 : a.u[static_cast<int64_t>(ri.b) * a.K + ri.t];
-    int32_t* outp = a.out_tokens + static_cast<int64_t>(ri.b) * a.K + ri.t;
-    if (bad || a.greedy) {
-      if (C.rank == 0 && tid == 0) {
-        const int tok = bad ? -1 : argmax;
-        *outp = tok;
-        rec->token = tok;
-      }
-    } else if (rank0_list || list_len >= 0) {
-      // kept list stored: draw over it (rank 0)
-      if (!rank0_list) { __threadfence(); }
-      C.cl.sync();  // lists written by every CTA are visible after the barrier
-      if (C.rank == 0) {
-        const int pos = list_ordered_draw(list_len, u, sm, [&](int i) { return __ldcg(&lw[i]); });
-        if (tid == 0) {
-          const int tok = (pos >= 0) ? __ldcg(&lidx[pos]) : -1;
-          *outp = tok;
-          rec->token = tok;
-        }
-      }
+    int tok;
+    if (bad) {
+      tok = -1;
+    } else if (a.greedy) {
+      tok = argmax;
+    } else if (list_len >= 0) {
+      __syncthreads();
+      const int pos = list_ordered_draw(list_len, u, sm, [&](int i) { return __ldcg(&lw[i]); });
+      tok = (pos >= 0) ? __ldcg(&lidx[pos]) : -1;
     } else {
-      // no stored list: ordered draw over the resident row
-      auto wk = [&](float l, int x) { return cut.keep(l, x) ? wexp(l, rc.m, rc.c) : 0.0f; };
-      // unfiltered rows: the totals of the normaliser pass are still in the mirror
-      if (use_k || use_p) (void)cluster_weight_total<E>(rc, sm, C, wk);
-      cluster_ordered_draw<E>(rc, sm, C, u, wk, [&](int tok) {
-        *outp = tok;
-        rec->token = tok;
-      });
+      tok = global_rows_draw<E>(a, grow, grow, m, m, cut, cut, 1.0f, 1.0f, false, u, sm);
+    }
+    if (tid == 0) {
+      a.out_tokens[static_cast<int64_t>(ri.b) * a.K + ri.t] = tok;
+      rec->token = tok;
     }
   }
 
-  // row record (rank 0)
-  if (C.rank == 0 && tid == 0) {
+  // row record
+  if (tid == 0) {
     int flags = 0;
-    if (bad) flags |= abort_ ? kFlagTimeout : kFlagNonfinite;
+    if (bad) flags |= kFlagNonfinite;
     double p_tok = 0.0;
     if (a.mode == kModeVerify && ri.t < a.K) {
-      const int d = ri.tok;
+      const int d = a.tokens[static_cast<int64_t>(ri.b) * a.K + ri.t];
       if (d < 0 || d >= a.V) {
         flags |= kFlagToken;
       } else if (!bad && !a.greedy) {
-        const float ld = Fmt<E>::at_global(rc.g, d);
+        const float ld = Fmt<E>::at_global(grow, d);
         // same weight as the kept list and the normaliser use
-        if (cut.keep(ld, d) && ld > -INFINITY) p_tok = static_cast<double>(wexp(ld, rc.m, rc.c)) / ff_to_d(zf);
+        if (cut.keep(ld, d) && ld > -INFINITY) p_tok = static_cast<double>(wexp(ld, m, a.c)) / ff_to_d(zf);
       }
     }
     rec->zf = ff_to_d(zf);
     rec->p_tok = p_tok;
-    rec->m = rc.m;
+    rec->m = m;
     rec->tau_val = cut.tv;
     rec->tau_idx = cut.ti;
     rec->argmax = argmax;
     rec->list_len = list_len;
     rec->flags = flags;
-    if (a.mode == kModeSample && (flags & ~kFlagToken)) set_status(a, abort_ ? SPEC_ERR_TIMEOUT : SPEC_ERR_NONFINITE);
+    if (a.mode == kModeSample && bad) set_status(a, SPEC_ERR_NONFINITE);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// segment phase helpers
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Streaming 16-byte load: read once, so no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& q, int w) {
+  return w == 0 ? q.x : w == 1 ? q.y : w == 2 ? q.z : q.w;
+}
+
+template <typename E>
+struct Seg;
+
+template <>
+struct Seg<uint16_t> {  // bf16 bits, 8 per vector
+  static constexpr int N = 8;
+  __device__ static float get(const uint4& q, int i) {
+    const uint32_t w = word_of(q, i >> 1);
+    return (i & 1) ? __uint_as_float(w & 0xffff0000u) : __uint_as_float(w << 16);
+  }
+  __device__ static uint4 neg_inf() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
+  // vector v with only its first n elements read (tail, or a row start that is
+  // not 16-byte aligned); the rest are -inf
+  __device__ static uint4 load_some(const uint16_t* g, int v, int n) {
+    const unsigned short* s = reinterpret_cast<const unsigned short*>(g) + static_cast<int64_t>(v) * 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = (2 * i < n) ? __ldg(s + 2 * i) : 0xff80u;
+      const uint32_t hi = (2 * i + 1 < n) ? __ldg(s + 2 * i + 1) : 0xff80u;
+      w[i] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  // NaN-propagating max of the vector, on packed pairs
+  __device__ static float vmax(const uint4& q) {
+    __nv_bfloat162 a, b, c, d;
+    memcpy(&a, &q.x, 4);
+    memcpy(&b, &q.y, 4);
+    memcpy(&c, &q.z, 4);
+    memcpy(&d, &q.w, 4);
+    const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+    uint32_t mw;
+    memcpy(&mw, &m, 4);
+    return max_nan(__uint_as_float(mw << 16), __uint_as_float(mw & 0xffff0000u));
+  }
+};
+
+template <>
+struct Seg<float> {  // 4 per vector
+  static constexpr int N = 4;
+  __device__ static float get(const uint4& q, int i) { return __uint_as_float(word_of(q, i)); }
+  __device__ static uint4 neg_inf() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
+  __device__ static uint4 load_some(const float* g, int v, int n) {
+    const float* s = g + static_cast<int64_t>(v) * 4;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = (i < n) ? __float_as_uint(__ldg(s + i)) : 0xff800000u;
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __device__ static float vmax(const uint4& q) {
+    return max_nan(max_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
+                   max_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
+  }
+};
+
+// A segment's top k in rank order from its n <= 32 R staged candidates; returns
+// (on every lane) the k-th value when there are k, else -inf.
+template <int R>
+__device__ float seg_topk_list(Scratch& sm, int n, int k, uint2* gc, int lane) {
+  unsigned long long key[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int i = lane * R + r;
+    key[r] = (i < n) ? sort_key(sm.cand_val[i], sm.cand_idx[i]) : 0ull;
+  }
+  warp_sort_keys_desc<R>(key, lane);
+  float kth = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int i = lane * R + r;
+    if (i < n && i < k) gc[i] = make_uint2(static_cast<uint32_t>(skey_idx(key[r])), __float_as_uint(skey_val(key[r])));
+    if (i < n && i == k - 1) kth = skey_val(key[r]);
+  }
+  return __shfl_sync(FULL, kth, ((k - 1) / R) & 31);
+}
+
+// ---------------------------------------------------------------------------
+// Counters in the workspace's counter area: every call finds them at zero and
+// leaves them at zero -- the arrival that completes a counter resets it, once
+// no other arrival of the call can touch it.
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// The two launches of a call.
+//
+// spec_seg_kernel: a persistent grid over items (item = row * nseg + segment);
+// CTA b takes items b, b + grid, b + 2 grid, ...  Each CTA owns two segment
+// buffers in shared memory that bulk copies fill two items ahead, so one copy is
+// in flight while an item is processed.  Per item: maxima, then (one barrier)
+// argmax, normaliser and the candidate floor, then (a second) the candidates,
+// then (a third) warp 0 writes the segment's list and record while the other
+// warps start the next item.
+//
+// spec_row_kernel: one CTA per row merges the row's segment records and lists,
+// cuts, records the row and -- for the last row of a sequence to finish, found
+// by a counter -- runs the sequence's accept tests and final draw.
+
+template <typename E>
+__device__ __forceinline__ const E* item_src(const KArgs& a, int item, int* s0, int* L) {
+  const int row = item / a.nseg, seg = item - row * a.nseg;
+  const RowInfo ri = decode_job(a, row);
+  *s0 = seg * a.S;
+  *L = min(a.S, a.V - *s0);
+  return static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off + *s0;
+}
+
+// Thread 0: start the bulk copy of an item's 16-byte-aligned part into a
+// segment buffer (one arrival with its byte count; a zero count completes the
+// phase at once).
+template <typename E>
+__device__ __forceinline__ void item_issue(const KArgs& a, int item, void* segbuf, uint64_t* bar) {
+  int s0, L;
+  const E* g = item_src<E>(a, item, &s0, &L);
+  const uint32_t bytes = static_cast<uint32_t>(L) * sizeof(E) & ~15u;
+  mbar_expect_tx(bar, bytes);
+  if (bytes > 0) bulk_copy_g2s(segbuf, g, bytes, bar);
+}
+
+// Vector v of an item: from the segment buffer when staged, else from global
+// memory (rows not 16-byte aligned, or after a lost copy); the partial tail
+// vector from global memory; -inf past the end.
+template <typename E>
+__device__ __forceinline__ uint4 item_vec(const E* g, int L, bool staged, bool aligned, const uint4* seg, int v) {
+  constexpr int N = Seg<E>::N;
+  if (v < L / N) {
+    if (staged) return seg[v];
+    if (aligned) return ld_stream(reinterpret_cast<const uint4*>(g) + v);
+  }
+  if (v * N < L) return Seg<E>::load_some(g, v, min(N, L - v * N));
+  return Seg<E>::neg_inf();
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
+  unsigned char* bufs = smem_raw + sizeof(Scratch);
+  constexpr int N = Seg<E>::N;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nitems = a.nrows * a.nseg;
+  const int grid = static_cast<int>(gridDim.x);
+  const int first = static_cast<int>(blockIdx.x);
+
+  // a bulk copy needs 16-byte-aligned rows; a copy that misses its bounded wait
+  // switches the CTA to plain loads (the stray copy is awaited before exit)
+  bool staged = a.aligned != 0;
+  bool issued0 = false, issued1 = false, stray0 = false, stray1 = false;
+  uint32_t ph0 = 0, ph1 = 0;
+  if (tid == 0) {
+    mbar_init(&sm.bar[0], 1);
+    mbar_init(&sm.bar[1], 1);
+    fence_mbar_init();
+    sm.seg_n = 0;
+    sm.theta = -INFINITY;
+  }
+  __syncthreads();
+  if (staged) {
+    issued0 = first < nitems;
+    issued1 = first + grid < nitems;
+    if (tid == 0) {
+      if (issued0) item_issue<E>(a, first, bufs, &sm.bar[0]);
+      if (issued1) item_issue<E>(a, first + grid, bufs + a.seg_bytes, &sm.bar[1]);
+    }
   }
 
-  // every global write of this cluster is ordered before the sequence ticket, and
-  // no CTA leaves while another may still read its shared memory
-  __threadfence();
-  C.cl.sync();
+  int k = 0;
+  for (int cur = first; cur < nitems; cur += grid, ++k) {
+    const int p = k & 1;
+    int s0, L;
+    const E* g = item_src<E>(a, cur, &s0, &L);
+    const uint4* seg = reinterpret_cast<const uint4*>(bufs + p * a.seg_bytes);
 
-  if (a.mode == kModeVerify && C.rank == 0) {
-    if (tid == 0) {
-      // Tagged ticket: a value left by an earlier call (other tag) counts as zero,
-      // so the workspace never needs re-zeroing.  Lock-free: a failed CAS means
-      // another row of this sequence finished, so at most R - 1 retries.
-      unsigned long long* tk = &a.tickets[ri.b];
-      const unsigned long long tag = static_cast<unsigned long long>(a.tag) << 32;
-      unsigned long long cur = atomicAdd(tk, 0ull), next;
-      for (int tries = 0; tries <= a.R; ++tries) {
-        next = ((cur & 0xffffffff00000000ull) == tag) ? cur + 1 : (tag | 1ull);
-        const unsigned long long seen = atomicCAS(tk, cur, next);
-        if (seen == cur) break;
-        cur = seen;
+    // ---- wait for this item's copy
+    const bool issued = p ? issued1 : issued0;
+    bool lost = false;
+    if (issued) {
+      uint32_t& ph = p ? ph1 : ph0;
+      lost = !mbar_wait_bounded(&sm.bar[p], ph);
+      ph ^= 1u;
+      if (lost) { if (p) stray1 = true; else stray0 = true; }
+    }
+    const bool from_smem = issued && !lost;
+    auto vec = [&](int j) { return item_vec<E>(g, L, from_smem, a.aligned != 0, seg, j * kThreads + tid); };
+
+    // ---- pass 1: per-vector and per-thread maxima (NaN-propagating)
+    float vm[kNV];
+    float tm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kNV; ++j) {
+      vm[j] = Seg<E>::vmax(vec(j));
+      tm = max_nan(tm, vm[j]);
+    }
+    float wm = tm;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wm = max_nan(wm, __shfl_xor_sync(FULL, wm, o));
+    if (lane == 0) sm.wf[warp] = wm;
+    sm.tmax[tid] = tm;
+    if (__syncthreads_or(lost)) staged = false;  // S1
+    float ms = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) ms = max_nan(ms, sm.wf[w]);
+    const bool bad = !(ms == ms) || ms == INFINITY;
+    const bool live = !bad && ms > -INFINITY;  // some finite value
+
+    // ---- first argmax: the first vector whose maximum is ms, then its first element
+    int am = INT_MAX;
+    if (live && tm == ms) {
+      int jj = 0;
+#pragma unroll
+      for (int j = kNV - 1; j >= 0; --j)
+        if (vm[j] == ms) jj = j;
+      const uint4 q = vec(jj);
+#pragma unroll
+      for (int i = N - 1; i >= 0; --i)
+        if (Seg<E>::get(q, i) == ms) am = (jj * kThreads + tid) * N + i;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = min(am, __shfl_xor_sync(FULL, am, o));
+    if (lane == 0) sm.wi[warp] = am;
+
+    // ---- normaliser relative to the segment max: pairwise within the thread,
+    // float-float across threads
+    if (a.need_z && live) {
+      float sv[kNV];
+#pragma unroll
+      for (int j = 0; j < kNV; ++j) {
+        const uint4 q = vec(j);
+        float w[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = wexp(Seg<E>::get(q, i), ms, a.c);
+#pragma unroll
+        for (int h = N / 2; h > 0; h >>= 1)
+#pragma unroll
+          for (int i = 0; i < h; ++i) w[i] += w[i + h];
+        sv[j] = w[0];
       }
-      sm.bi[15] = (next == (tag | static_cast<unsigned long long>(a.R)));
-      __threadfence();
+#pragma unroll
+      for (int h = 1; h < kNV; h <<= 1)
+#pragma unroll
+        for (int j = 0; j + h < kNV; j += 2 * h) sv[j] += sv[j + h];
+      const FF wz = warp_sum_ff(ff(sv[0]));
+      if (lane == 0) sm.wd[warp] = wz;
+    }
+
+    // ---- candidate floor: the n0-th largest thread maximum.  Each thread ranks
+    // its maximum among all kThreads under (value desc, thread asc); exactly one
+    // thread has rank n0 - 1.
+    const bool cands = a.filt && live && a.n0 <= kThreads;
+    if (cands) {
+      int rank = 0;
+      const float4* t4 = reinterpret_cast<const float4*>(sm.tmax);
+#pragma unroll 8
+      for (int q = 0; q < kThreads / 4; ++q) {
+        const float4 v = t4[q];
+        const int u = 4 * q;
+        rank += (v.x > tm || (v.x == tm && u < tid)) ? 1 : 0;
+        rank += (v.y > tm || (v.y == tm && u + 1 < tid)) ? 1 : 0;
+        rank += (v.z > tm || (v.z == tm && u + 2 < tid)) ? 1 : 0;
+        rank += (v.w > tm || (v.w == tm && u + 3 < tid)) ? 1 : 0;
+      }
+      if (rank == a.n0 - 1) sm.theta = tm;
+    }
+    __syncthreads();  // S2
+
+    // ---- candidates: every finite element >= theta, from the vectors whose
+    // maximum reaches it, staged in the candidate arrays
+    const float theta = sm.theta;
+    if (cands && tm >= theta) {
+      uint32_t mask = 0;
+#pragma unroll
+      for (int j = 0; j < kNV; ++j)
+        if (vm[j] >= theta) mask |= 1u << j;
+      while (mask) {
+        const int j = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const uint4 q = vec(j);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+          const float x = Seg<E>::get(q, i);
+          if (x >= theta && x > -INFINITY) {
+            const int pos = atomicAdd(&sm.seg_n, 1);
+            if (pos < kSegCap) {
+              sm.cand_idx[pos] = s0 + (j * kThreads + tid) * N + i;
+              sm.cand_val[pos] = x;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();  // S3: the buffer and the candidates are complete
+
+    // ---- refill the buffer with the item two ahead
+    const int nxt = cur + 2 * grid;
+    const bool refill = staged && nxt < nitems;
+    if (p) issued1 = refill; else issued0 = refill;
+    if (tid == 0 && refill) {
+      fence_proxy_async_smem();
+      item_issue<E>(a, nxt, bufs + p * a.seg_bytes, &sm.bar[p]);
+    }
+
+    // ---- warp 0: the segment's list and record; the other warps go on
+    if (warp == 0) {
+      const int n = sm.seg_n;
+      const bool over = a.filt && live && (!cands || n > kSegCap);
+      const bool use_k = a.top_k > 0;
+      uint2* gc = a.seg_cand + static_cast<int64_t>(cur) * kSegCap;
+      float kth = -INFINITY;
+      if (cands && !over) {
+        if (use_k) {
+          if (n <= 64) kth = seg_topk_list<2>(sm, n, a.top_k, gc, lane);
+          else if (n <= 128) kth = seg_topk_list<4>(sm, n, a.top_k, gc, lane);
+          else kth = seg_topk_list<8>(sm, n, a.top_k, gc, lane);
+        } else {
+          for (int c = lane; c < n; c += 32)
+            gc[c] = make_uint2(static_cast<uint32_t>(sm.cand_idx[c]), __float_as_uint(sm.cand_val[c]));
+        }
+      }
+      if (lane == 0) {
+        int amin = INT_MAX;
+        for (int w = 0; w < kWarps; ++w) amin = min(amin, sm.wi[w]);
+        FF z = ff(0.0f);
+        if (a.need_z && live)
+          for (int w = 0; w < kWarps; ++w) z = ff_add(z, sm.wd[w]);
+        SegRec r;
+        r.m = ms;
+        r.argmax = (amin == INT_MAX) ? -1 : s0 + amin;
+        r.z_hi = z.hi;
+        r.z_lo = z.lo;
+        r.theta = cands ? theta : -INFINITY;
+        r.kth = (cands && !over && use_k && n >= a.top_k) ? kth : -INFINITY;
+        r.ncand = (cands && !over) ? (use_k ? min(n, a.top_k) : n) : 0;
+        r.flags = (bad ? kSegBad : 0) | (over ? kSegOver : 0);
+        r.off = 0;
+        r.pad_[0] = r.pad_[1] = r.pad_[2] = 0;
+        a.segs[cur] = r;
+        sm.seg_n = 0;  // the next item's candidates (its first barrier orders this)
+        sm.theta = -INFINITY;
+      }
+    }
+  }
+  // copies that missed their wait must land before the shared memory is released
+  if (stray0) (void)mbar_wait_bounded(&sm.bar[0], ph0 ^ 1u);
+  if (stray1) (void)mbar_wait_bounded(&sm.bar[1], ph1 ^ 1u);
+}
+
+// Row merge, cut, record and (verify) the sequence counter and epilogue.
+template <typename E>
+__global__ void __launch_bounds__(kThreads) spec_row_kernel(const KArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
+  unsigned char* scratch = smem_raw + sizeof(Scratch);
+  int32_t* pool_idx = reinterpret_cast<int32_t*>(scratch);
+  float* pool_val = reinterpret_cast<float*>(pool_idx + kPool);
+  const SortBuf sb{reinterpret_cast<unsigned long long*>(pool_val + kPool)};
+  for (int row = static_cast<int>(blockIdx.x); row < a.nrows; row += static_cast<int>(gridDim.x)) {
+    const RowInfo ri = decode_job(a, row);
+    const E* grow = static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off;
+    row_merge(a, row, sm, sb, pool_idx, pool_val);
+    Local C;
+    row_finish<E>(a, ri, grow, sm, C, sb, pool_idx, pool_val);
+    // every global write of the row is ordered before the sequence counter
+    __syncthreads();
+    if (a.mode == kModeVerify) {
+      if (threadIdx.x == 0) {
+        fence_acq_rel_gpu();
+        unsigned long long* tk = &a.tickets[ri.b];
+        const bool last = atomicAdd(tk, 1ull) == static_cast<unsigned long long>(a.R - 1);
+        if (last) {
+          *tk = 0ull;  // the sequence's last row: no other arrival of this call
+          fence_acq_rel_gpu();
+        }
+        sm.bi[15] = last ? 1 : 0;
+      }
+      __syncthreads();
+      if (sm.bi[15]) verify_epilogue<E>(a, ri.b, sm);
     }
     __syncthreads();
-    if (sm.bi[15]) verify_epilogue<E>(a, ri.b, sm);
   }
 }
 
@@ -1812,18 +2132,12 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const KArgs a) {
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
-std::atomic<uint32_t> g_tag{0};
-
-uint32_t next_tag() {
-  uint32_t t;
-  do { t = g_tag.fetch_add(1, std::memory_order_relaxed) + 1; } while (t == 0);
-  return t;
-}
 
 struct DevInfo {
   int sms = 0;
   int max_smem = 0;
-  size_t smem_set[2] = {0, 0};  // dynamic smem attribute already set, per kernel
+  size_t smem_set[4] = {0, 0, 0, 0};  // dynamic smem attribute set: [kernel * 2 + dtype]
+  int per_sm[2] = {0, 0};              // resident segment-kernel CTAs per SM, per dtype
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
@@ -1845,17 +2159,20 @@ bool dev_info(DevInfo** out) {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Plan {
-  int esize = 0, R = 0, CS = 1, S = 0, aligned = 0;
-  int64_t nrows = 0;
-  size_t smem = 0;
-  size_t off_tickets = 0, off_rows = 0, off_lidx = 0, off_lw = 0, ws_bytes = 0;
+  int esize = 0, R = 0, S = 0, nseg = 0, n0 = 0, grid = 0, row_grid = 0, seg_bytes = 0;
+  bool clear_counters = false;  // more counters than the area that calls keep zeroed
+  size_t counter_bytes = 0;
+  int64_t nrows = 0, items = 0;
+  size_t smem = 0, row_smem = 0;  // dynamic shared memory of the segment and row kernels
+  size_t off_tickets = 0, off_rows = 0, off_lidx = 0, off_lw = 0, off_segs = 0, off_cand = 0, ws_bytes = 0;
 };
 
 bool finite_positive(float x) { return x > 0.0f && x < INFINITY; }
 
-// Validates the parameters shared by both entry points and sizes the workspace.
-// Cluster/slice choice needs the device; with `need_device` false only sizes are
-// computed (used by the *_workspace_size queries, which then do not touch CUDA).
+// Validates the parameters shared by both entry points, cuts rows into equal
+// segments of at most kNV vectors per thread and sizes the workspace -- all
+// from the parameters alone (no CUDA call), so the *_workspace_size queries work
+// without a device.
 spec_status make_plan(const spec_params* p, bool verify, Plan* pl) {
   if (!p) return SPEC_ERR_INVALID_ARG;
   if (p->B < 0 || p->K < 1 || p->V < 1) return SPEC_ERR_INVALID_ARG;
@@ -1871,99 +2188,131 @@ spec_status make_plan(const spec_params* p, bool verify, Plan* pl) {
   pl->esize = (p->dtype == SPEC_F32) ? 4 : 2;
   pl->R = verify ? (p->greedy ? p->K + 1 : 2 * p->K + 1) : p->K;
   pl->nrows = static_cast<int64_t>(p->B) * pl->R;
-  if (pl->nrows > (int64_t(1) << 27)) return SPEC_ERR_INVALID_ARG;
+  if (pl->nrows > (int64_t(1) << 30)) return SPEC_ERR_INVALID_ARG;
+  const int64_t V = p->V;
+  const int64_t N = 16 / pl->esize;  // elements per 16-byte vector
+  const int64_t smax = static_cast<int64_t>(kNV) * kThreads * N;
+  int64_t nseg = (V + smax - 1) / smax;
+  int64_t S = (V + nseg - 1) / nseg;
+  S = (S + N - 1) / N * N;
+  nseg = (V + S - 1) / S;
+  pl->S = static_cast<int>(S);
+  pl->nseg = static_cast<int>(nseg);
+  pl->items = pl->nrows * nseg;
+  if (pl->items > INT_MAX) return SPEC_ERR_UNSUPPORTED;
+  // candidate floor rank: a segment's top-k for top-k; for top-p alone a floor
+  // whose candidates (about 1.4 n0 per segment) leave the row's pool room
+  const bool use_k = !p->greedy && p->top_k > 0 && p->top_k < p->V;
+  const bool use_p = !p->greedy && p->top_p < 1.0f;
+  pl->n0 = use_k ? p->top_k : use_p ? static_cast<int>(std::min<int64_t>(128, std::max<int64_t>(16, 560 / nseg))) : 0;
+  // segment kernel: two segment buffers; row kernel: the pool, its sort keys and
+  // the merge's entry table
+  pl->seg_bytes = static_cast<int>(round_up(static_cast<size_t>(S) * pl->esize, 128));
+  pl->smem = sizeof(Scratch) + 2 * static_cast<size_t>(pl->seg_bytes);
+  pl->row_smem = sizeof(Scratch) + kPool * (sizeof(int32_t) + sizeof(float) + sizeof(unsigned long long)) + kListTable;
+  const size_t nr = static_cast<size_t>(pl->nrows);
+  const size_t ni = static_cast<size_t>(pl->items);
+  // the counter area: at offset 0 and at least kCounterArea bytes, so that a
+  // later call with another layout still finds the zeros this call leaves
+  const size_t counters = static_cast<size_t>(p->B) * sizeof(unsigned long long);
   pl->off_tickets = 0;
-  pl->off_rows = round_up(static_cast<size_t>(p->B) * 8, 256);
-  pl->off_lidx = pl->off_rows + round_up(static_cast<size_t>(pl->nrows) * sizeof(spec_row_stat), 256);
-  pl->off_lw = pl->off_lidx + round_up(static_cast<size_t>(pl->nrows) * kCap * 4, 256);
-  pl->ws_bytes = pl->off_lw + round_up(static_cast<size_t>(pl->nrows) * kCap * 4, 256);
+  pl->counter_bytes = counters;
+  pl->clear_counters = counters > kCounterArea;
+  pl->off_rows = std::max(kCounterArea, round_up(counters, 256));
+  pl->off_lidx = pl->off_rows + round_up(nr * sizeof(spec_row_stat), 256);
+  pl->off_lw = pl->off_lidx + round_up(nr * kCap * 4, 256);
+  pl->off_segs = pl->off_lw + round_up(nr * kCap * 4, 256);
+  pl->off_cand = pl->off_segs + round_up(ni * sizeof(SegRec), 256);
+  // candidate lists whenever sampling (the size must not depend on top-k / top-p)
+  pl->ws_bytes = pl->off_cand + (p->greedy ? 0 : round_up(ni * kSegCap * sizeof(uint2), 256));
   return SPEC_OK;
 }
 
-// Slice and cluster size: ~64 KB of row per CTA (three CTAs per SM), smaller
-// slices while there are fewer than two CTAs per SM, at most 8 CTAs per row.
-spec_status plan_launch(const spec_params* p, const DevInfo& di, Plan* pl) {
-  const int64_t row_bytes = static_cast<int64_t>(p->V) * pl->esize;
-  int64_t target = 65536;
-  const int64_t jobs = pl->nrows;
-  while (target > 8192 && jobs * std::min<int64_t>(kMaxCluster, (row_bytes + target - 1) / target) <
-                              2 * static_cast<int64_t>(di.sms))
-    target /= 2;
-  int cs = static_cast<int>(std::min<int64_t>(kMaxCluster, std::max<int64_t>(1, (row_bytes + target - 1) / target)));
-  for (;;) {
-    int64_t S = (static_cast<int64_t>(p->V) + cs - 1) / cs;
-    S = (S + 63) / 64 * 64;
-    const int real_cs = static_cast<int>((p->V + S - 1) / S);
-    const size_t smem = sizeof(Scratch) + std::max(kSortBufBytes, round_up(static_cast<size_t>(S) * pl->esize, 128));
-    if (smem <= static_cast<size_t>(di.max_smem)) {
-      pl->CS = real_cs;
-      pl->S = static_cast<int>(S);
-      pl->smem = smem;
-      return SPEC_OK;
-    }
-    if (cs >= kMaxCluster) return SPEC_ERR_UNSUPPORTED;
-    ++cs;
+template <typename E>
+const void* seg_fn() { return reinterpret_cast<const void*>(&spec_seg_kernel<E>); }
+template <typename E>
+const void* row_fn() { return reinterpret_cast<const void*>(&spec_row_kernel<E>); }
+
+spec_status set_smem(DevInfo& di, int slot, const void* fn, size_t bytes) {
+  if (di.smem_set[slot] >= bytes) return SPEC_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess ||
+      cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  di.smem_set[slot] = bytes;
+  return SPEC_OK;
+}
+
+// Segment kernel: a persistent grid, as many CTAs as fit at once (never more
+// than the items).  Row kernel: one CTA per row.
+spec_status plan_launch(const spec_params* p, DevInfo& di, Plan* pl) {
+  if (pl->smem > static_cast<size_t>(di.max_smem) || pl->row_smem > static_cast<size_t>(di.max_smem))
+    return SPEC_ERR_UNSUPPORTED;
+  const int which = (p->dtype == SPEC_F32) ? 0 : 1;
+  const void* fs = which == 0 ? seg_fn<float>() : seg_fn<uint16_t>();
+  const void* fr = which == 0 ? row_fn<float>() : row_fn<uint16_t>();
+  std::lock_guard<std::mutex> lock(g_mu);
+  const size_t before = di.smem_set[which];
+  spec_status s = set_smem(di, which, fs, pl->smem);
+  if (s != SPEC_OK) return s;
+  s = set_smem(di, 2 + which, fr, pl->row_smem);
+  if (s != SPEC_OK) return s;
+  if (di.per_sm[which] == 0 || di.smem_set[which] != before) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fs, kThreads, pl->smem) != cudaSuccess || per_sm < 1)
+      return SPEC_ERR_CUDA;
+    di.per_sm[which] = per_sm;
   }
+  pl->grid = static_cast<int>(std::min<int64_t>(pl->items, static_cast<int64_t>(di.per_sm[which]) * di.sms));
+  pl->row_grid = static_cast<int>(std::min<int64_t>(pl->nrows, int64_t(1) << 20));
+  return SPEC_OK;
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 spec_status launch(const spec_params* p, const Plan& pl, KArgs& a, DevInfo* di) {
+  (void)di;
   if (pl.nrows == 0) return SPEC_OK;
-  const int which = (p->dtype == SPEC_F32) ? 0 : 1;
-  const void* fn = which == 0 ? reinterpret_cast<const void*>(&spec_rows_kernel<float>)
-                              : reinterpret_cast<const void*>(&spec_rows_kernel<uint16_t>);
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (di->smem_set[which] < pl.smem) {
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) !=
-          cudaSuccess)
-        return SPEC_ERR_CUDA;
-      di->smem_set[which] = pl.smem;
-    }
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(pl.nrows * pl.CS), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = pl.smem;
-  cfg.stream = static_cast<cudaStream_t>(p->stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(pl.CS);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t err;
-  if (which == 0)
-    err = cudaLaunchKernelEx(&cfg, spec_rows_kernel<float>, a);
-  else
-    err = cudaLaunchKernelEx(&cfg, spec_rows_kernel<uint16_t>, a);
-  if (err != cudaSuccess) {
-    (void)cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(pl.grid)), rgrid(static_cast<unsigned>(pl.row_grid)), block(kThreads);
+  cudaStream_t st = static_cast<cudaStream_t>(p->stream);
+  if (pl.clear_counters && cudaMemsetAsync(p->workspace, 0, pl.counter_bytes, st) != cudaSuccess)
     return SPEC_ERR_CUDA;
+  if (p->dtype == SPEC_F32) {
+    spec_seg_kernel<float><<<grid, block, pl.smem, st>>>(a);
+    spec_row_kernel<float><<<rgrid, block, pl.row_smem, st>>>(a);
+  } else {
+    spec_seg_kernel<uint16_t><<<grid, block, pl.smem, st>>>(a);
+    spec_row_kernel<uint16_t><<<rgrid, block, pl.row_smem, st>>>(a);
   }
-  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  g_launches.fetch_add(2, std::memory_order_relaxed);
   return SPEC_OK;
 }
 
 void fill_common(const spec_params* p, const Plan& pl, KArgs& a) {
   char* ws = static_cast<char*>(p->workspace);
   a.tickets = reinterpret_cast<unsigned long long*>(ws + pl.off_tickets);
-  a.tag = next_tag();
   a.rows = reinterpret_cast<spec_row_stat*>(ws + pl.off_rows);
   a.list_idx = reinterpret_cast<int32_t*>(ws + pl.off_lidx);
   a.list_w = reinterpret_cast<float*>(ws + pl.off_lw);
+  a.segs = reinterpret_cast<SegRec*>(ws + pl.off_segs);
+  a.seg_cand = reinterpret_cast<uint2*>(ws + pl.off_cand);
   a.B = p->B;
   a.K = p->K;
   a.V = p->V;
   a.R = pl.R;
   a.S = pl.S;
+  a.nseg = pl.nseg;
+  a.seg_bytes = pl.seg_bytes;
+  a.nrows = static_cast<int>(pl.nrows);
   a.greedy = p->greedy ? 1 : 0;
   a.top_k = (p->greedy || p->top_k >= p->V) ? 0 : p->top_k;
   a.top_p = p->greedy ? 1.0f : p->top_p;
   a.temp = p->greedy ? 1.0f : p->temperature;
   a.c = p->greedy ? 1.0f : static_cast<float>(1.4426950408889634 / static_cast<double>(p->temperature));
+  const bool use_k = a.top_k > 0, use_p = a.top_p < 1.0f;
+  a.filt = (!p->greedy && (use_k || use_p)) ? 1 : 0;
+  a.need_z = (!p->greedy && !use_k) ? 1 : 0;
+  a.n0 = pl.n0;
   a.status = p->status;
 }
 
@@ -2073,8 +2422,8 @@ const char* spec_status_string(spec_status status) {
     case SPEC_ERR_CUDA: return "CUDA runtime error";
     case SPEC_ERR_NONFINITE: return "non-finite logits (NaN, +inf, or no finite value in a row)";
     case SPEC_ERR_TOKEN_RANGE: return "draft token outside [0, V)";
-    case SPEC_ERR_TIMEOUT: return "bounded wait on an asynchronous copy ran out";
-    case SPEC_ERR_UNSUPPORTED: return "vocabulary too large for one row per thread-block cluster";
+    case SPEC_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    case SPEC_ERR_UNSUPPORTED: return "problem too large for one launch (rows x segments, or shared memory)";
     case SPEC_ERR_SCRATCH_LIMIT: return "request needs more scratch than spec_verify_noalloc's fixed array";
   }
   return "unknown status";

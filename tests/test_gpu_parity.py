@@ -215,6 +215,31 @@ def test_repeatable_bit_for_bit(sv):
         assert np.array_equal(o[0], outs[0][0]) and np.array_equal(o[1], outs[0][1])
 
 
+def test_workspace_shared_across_shapes(sv):
+    """One zero-filled workspace serves calls of different shapes and modes: every
+    call leaves the counter area (its first 64 KB) at zero, and the results of a
+    call after the others still match the oracle."""
+    ws = torch.zeros(48 << 20, dtype=torch.uint8, device=DEV)
+    cases = [("c5", dict(B=3)), ("c3", dict(B=6, V=50001)), ("c2", {}), ("c4", dict(B=16)),
+             ("c1", {}), ("c5", dict(B=2, V=70003))]
+    for name, kw in cases:
+        w = workloads.make(name, **kw)
+        prm = params_of(w)
+        drf = to_dev(w["draft"])
+        tok = sv.spec_sample_draft(drf, None if w["greedy"] else to_dev(w["u_draft"]), ws=ws, **prm)
+        torch.cuda.synchronize()
+        assert int(ws[:65536].count_nonzero()) == 0, name
+        ref_d = oracle.sample_draft(w["draft"], w["u_draft"], **prm)
+        ok = ref_d["flags"] == 0
+        assert np.array_equal(tok.cpu().numpy()[ok], ref_d["tokens"][ok]), name
+        out_t, out_n = sv.spec_verify(to_dev(w["target"]), drf, to_dev(ref_d["tokens"]), to_dev(w["u_verify"]),
+                                      ws=ws, **prm)
+        torch.cuda.synchronize()
+        assert int(ws[:65536].count_nonzero()) == 0, name
+        ref = oracle.verify(w["target"], w["draft"], ref_d["tokens"], w["u_verify"], **prm)
+        compare_verify(out_t.cpu().numpy(), out_n.cpu().numpy(), ref, "shared-ws-" + name)
+
+
 def test_worked_example_distribution_on_gpu(sv):
     """"Speculative Decoding" (roadtointelligence.com), "Why the output doesn't change":
     acceptance 0.8 and emitted words in the target's proportions, not the draft's."""
