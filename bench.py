@@ -56,6 +56,24 @@ def workload_desc(name, w):
         else "%s: %s, Gaussian synthetic logits" % (name, cfg.describe())
 
 
+def recorded_traffic(workload):
+    """DRAM bytes (read + write) of one spec_verify call on this workload, as an
+    ncu capture recorded them in profiles/traffic.json -- only while the kernel
+    source is the one that was captured (else None)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, "speculative_sampling_verification_spec_gb300", "csrc", "spec_verify.cu")
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if rec.get("source_sha256") == sha and workload in rec.get("verify_bytes_per_call", {}):
+            return float(rec["verify_bytes_per_call"][workload])
+    except Exception:
+        pass
+    return None
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -380,8 +398,9 @@ def run_gpu(args, name):
                                               "gbs": bytes_s / (avg_s / 1e3) / 1e9,
                                               "rows_per_s": rs / (avg_s / 1e3)}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
-                         "kernel": "spec_rows_kernel (spec_verify)", "peak_kind": peak_kind},
+                         "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                         "kernel": "spec_seg_kernel + spec_row_kernel (one spec_verify call)",
+                         "peak_kind": peak_kind},
             "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
             "gpu_launches": int(r["launches"]),

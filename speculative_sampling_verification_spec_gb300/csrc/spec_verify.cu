@@ -239,7 +239,14 @@ __device__ __forceinline__ float okey32_val(uint32_t k) {
 }
 
 // weight of one logit relative to the row max m; c = log2(e)/T
-__device__ __forceinline__ float wexp(float l, float m, float c) { return exp2f((l - m) * c); }
+// 2^x by the hardware approximation (relative error below 2^-22; results
+// below 2^-126 flush to zero)
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float wexp(float l, float m, float c) { return ex2f((l - m) * c); }
 
 // ---------------------------------------------------------------------------
 // float-float ("double-single") sums.  GB300 runs FP64 at a small fraction of
@@ -311,6 +318,8 @@ struct KArgs {
   uint2* seg_cand;      // [nrows * nseg * kSegCap]: (row index, logit bits)
   int B, K, V, R;       // R rows per sequence
   int S, nseg, nrows;   // S elements per segment (a multiple of the vector width)
+  uint32_t nseg_m, nseg_s;  // n / nseg == (umulhi(n, m) + n) >> s for 0 <= n < 2^31
+  uint32_t rows_m, rows_s;  // the same for rows per sequence (verify: R, sample: K)
   int seg_bytes;        // bytes of one segment buffer in shared memory
   int mode, greedy, top_k, aligned;
   int need_z;           // segments sum the normaliser (no filter, or top-p without top-k)
@@ -340,14 +349,16 @@ struct alignas(128) Scratch {
   alignas(16) float tmax[kThreads];  // per-thread maxima (read as float4)
   float theta, kth;
   int32_t seg_n, last;
+  int32_t seg_cnt[2];   // candidates of items k with k & 1 == 0, 1
   // the row being merged
+  unsigned long long row_bound;  // largest key a list head left out (0: none)
   FF row_z;
   float row_m, row_theta, row_kth;
   int32_t row_argmax, row_flags, row_over, pool_n;
   FF bd[kProbes + 4];
   int32_t bi[kProbes + 8];
   // candidates of the general path; the draft's kept list in the epilogue
-  int32_t cand_idx[kCap];
+  alignas(8) int32_t cand_idx[kCap];  // segment kernel: kSegCap 64-bit candidate keys
   float cand_val[kCap];
 };
 
@@ -357,7 +368,7 @@ struct SortBuf {
 };
 static_assert(sizeof(Scratch) <= 8192, "shared scratch grew past its budget");
 static_assert(kCap % kThreads == 0 && kPool % kThreads == 0, "lists are split evenly over the threads");
-static_assert(kSegCap <= kCap, "a segment's candidates are staged in the candidate arrays");
+static_assert(kSegCap * 8 <= kCap * 4, "a segment's candidate keys are staged in cand_idx");
 static_assert(sizeof(SegRec) % 16 == 0, "segment records are moved as 16-byte words");
 static_assert(sizeof(Slot) % sizeof(uint32_t) == 0, "slots are copied as 32-bit words");
 static_assert(kThreads * sizeof(SegRec) <= kPool * sizeof(unsigned long long),
@@ -1500,17 +1511,24 @@ __device__ void write_kept_by_index(const unsigned long long* skey, int n, float
 
 // Fold the row's segment records into sm.row_*: max, first argmax, normaliser
 // (each segment's sum rescaled to the row max, float-float, fixed order),
-// flags, the largest theta and per-segment k-th value; then gather the
-// segments' lists into the pool.  Records are staged a tile at a time in the
-// sort-key buffer and folded by warp 0, 32 at a time.
-__device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int32_t* pidx, float* pval) {
+// flags, the largest theta and per-segment k-th value; then gather the first
+// `lim` entries of every segment's list (sorted: value desc, index asc) into
+// the pool, and in sm.row_bound the largest key left out of a list (0: none).
+// Top-k keeps only entries >= max(kfloor, every segment's k-th value): both
+// bound the row's k-th value from below.
+// Records are staged a tile at a time in the sort-key buffer and folded by
+// warp 0, 32 at a time.
+__device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int32_t* pidx, float* pval, int lim,
+                          float kfloor) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   SegRec* stage = reinterpret_cast<SegRec*>(sb.skey);
   const SegRec* recs = a.segs + static_cast<int64_t>(row) * a.nseg;
   const int ns = a.nseg;
   float m = -INFINITY, th = -INFINITY, kl = -INFINITY;
   int am = -1, fl = 0, total = 0;
+  unsigned long long bound = 0ull;
   FF z = ff(0.0f);
+  const uint2* cand = a.seg_cand + static_cast<int64_t>(row) * a.nseg * kSegCap;
   for (int t0 = 0; t0 < ns; t0 += kThreads) {
     const int nt = min(kThreads, ns - t0);
     __syncthreads();
@@ -1528,7 +1546,19 @@ __device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int3
         const int flags = valid ? stage[s].flags : 0;
         const bool good = valid && !(flags & kSegBad);
         const float ms = good ? stage[s].m : -INFINITY;
-        const int nc = valid ? stage[s].ncand : 0;
+        const int listed = valid ? stage[s].ncand : 0;
+        const int nc = min(listed, lim);
+        unsigned long long bk = 0ull;
+        if (listed > lim) {  // the first entry this list leaves out
+          const uint2 e = __ldcg(cand + static_cast<int64_t>(t0 + s) * kSegCap + lim);
+          bk = sort_key(__uint_as_float(e.y), static_cast<int>(e.x));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const unsigned long long ob = __shfl_xor_sync(FULL, bk, o);
+          bk = ob > bk ? ob : bk;
+        }
+        bound = bk > bound ? bk : bound;
         const int incl = warp_incl_scan_i(nc, lane);
         if (valid) stage[s].off = total + incl - nc;
         total += __shfl_sync(FULL, incl, 31);
@@ -1537,13 +1567,13 @@ __device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int3
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(FULL, cm, o));
         if (cm > m) {  // a new row max (uniform): rescale the sum so far
-          if (z.hi > 0.0f) z = ff_mul(z, exp2f((m - cm) * a.c));
+          if (z.hi > 0.0f) z = ff_mul(z, ex2f((m - cm) * a.c));
           m = cm;
           const unsigned hit = __ballot_sync(FULL, good && ms == cm);
           am = __shfl_sync(FULL, valid ? stage[s].argmax : -1, __ffs(hit) - 1);
         }
         FF zs = ff(0.0f);
-        if (good && stage[s].z_hi > 0.0f) zs = ff_mul(FF{stage[s].z_hi, stage[s].z_lo}, exp2f((ms - m) * a.c));
+        if (good && stage[s].z_hi > 0.0f) zs = ff_mul(FF{stage[s].z_hi, stage[s].z_lo}, ex2f((ms - m) * a.c));
         z = ff_add(z, warp_sum_ff(zs));
         float tv = good ? stage[s].theta : -INFINITY, kv = good ? stage[s].kth : -INFINITY;
 #pragma unroll
@@ -1562,6 +1592,7 @@ __device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int3
     sm.row_flags = fl;
     sm.row_theta = th;
     sm.row_kth = kl;
+    sm.row_bound = bound;
     sm.row_z = z;
     // the pool's segment offsets are staged for one tile only
     sm.row_over = (ns > kThreads) || (fl & kSegOver) || (a.top_k <= 0 && total > kPool);
@@ -1575,12 +1606,11 @@ __device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int3
   // whose offset is <= e.  Each thread issues up to eight loads at once.
   total = sm.pool_n;  // folded by warp 0
   if (a.filt && !sm.row_over && !(sm.row_flags & kSegBad) && total <= kListTable) {
-    const uint2* cand = a.seg_cand + static_cast<int64_t>(row) * a.nseg * kSegCap;
-    const float floor_v = (a.top_k > 0) ? sm.row_kth : -INFINITY;
+    const float floor_v = (a.top_k > 0) ? fmaxf(sm.row_kth, kfloor) : -INFINITY;
     // entry -> segment table (one byte per entry; ns <= kThreads <= 255)
     uint8_t* segof = reinterpret_cast<uint8_t*>(sb.skey + kPool);
     for (int s = tid; s < ns; s += kThreads)
-      for (int i = 0; i < stage[s].ncand; ++i) segof[stage[s].off + i] = static_cast<uint8_t>(s);
+      for (int i = 0, e = min(stage[s].ncand, lim); i < e; ++i) segof[stage[s].off + i] = static_cast<uint8_t>(s);
     __syncthreads();
     constexpr int U = 8;
     for (int base = 0; base < total; base += kThreads * U) {
@@ -1620,16 +1650,24 @@ __device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int3
 // Row end: exact cut from the pool (or the general path), record, draw.
 template <typename E>
 __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scratch& sm, Local& C, SortBuf sb,
-                           const int32_t* pool_idx, const float* pool_val) {
+                           int32_t* pool_idx, float* pool_val) {
   const int tid = threadIdx.x;
+  // first the pool of every segment list's head: as many entries as the
+  // 256-key register sort holds
+  const int row = ri.job;
+  const int ns = a.nseg;
+  int lim = (a.top_k > 0) ? min(a.top_k, max(4, 256 / ns)) : max(4, 256 / ns);
+  if (lim >= kSegCap) lim = INT_MAX;
+  row_merge(a, row, sm, sb, pool_idx, pool_val, lim, -INFINITY);
   const float m = sm.row_m;
   const int argmax = sm.row_argmax;
   const int fl = sm.row_flags;
   // NaN / +inf in a segment, or no finite value in the row
   const bool bad = (fl & kSegBad) || !(m > -INFINITY);
   const FF z = sm.row_z;
-  const bool over = sm.row_over != 0;
-  const int total = sm.pool_n;
+  bool over = sm.row_over != 0;
+  int total = sm.pool_n;
+  unsigned long long bound = sm.row_bound;
   const float theta = sm.row_theta;
   __syncthreads();
 
@@ -1653,12 +1691,34 @@ __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scr
   int list_len = -1;
   if (!bad && !a.greedy && (use_k || use_p)) {
     bool done = false;
-    if (!over && total > 0) {
+    float head_kth = -INFINITY;
+    for (int attempt = 0; attempt < 2 && !done; ++attempt) {
+      if (attempt == 1) {  // the heads did not settle the cut: every listed entry
+        if (lim == INT_MAX) break;
+        row_merge(a, row, sm, sb, pool_idx, pool_val, INT_MAX, head_kth);
+        over = sm.row_over != 0;
+        total = sm.pool_n;
+        bound = sm.row_bound;
+        __syncthreads();
+      }
+      if (over || total <= 0) continue;
       const CutResult res = sort_and_cut(m, a.c, pool_idx, pool_val, total, sb, use_k ? a.top_k : 0,
                                          use_p ? a.top_p : 1.0f, z, sm);
-      // exact when the pool holds the row's top-k, or when the top-p prefix
-      // closes at or above every segment's candidate floor
-      if (use_k || (res.reached && theta <= res.tv)) {
+      // Exact when no element outside the pool can be kept.  Every element
+      // left out of a list's head has a key <= bound; every element left out of
+      // a list lies below its segment's k-th value (top-k: the pool's k-th key
+      // must exceed bound), or below the segment's candidate floor (top-p: the
+      // cut must be reached within the pool, at or above every floor, and
+      // above bound).
+      bool exact;
+      if (use_k) {
+        // the head pool's k-th value bounds the row's k-th value from below
+        if (total >= a.top_k) head_kth = skey_val(sb.skey[a.top_k - 1]);
+        exact = bound == 0ull || (total >= a.top_k && sb.skey[a.top_k - 1] > bound);
+      } else {
+        exact = res.reached && theta <= res.tv && (bound == 0ull || sort_key(res.tv, res.ti) > bound);
+      }
+      if (exact) {
         cut = Cut{res.tv, res.ti};
         zf = res.zf;
         if (res.nkeep <= kCap) {
@@ -1798,25 +1858,31 @@ struct Seg<float> {  // 4 per vector
   }
 };
 
-// A segment's top k in rank order from its n <= 32 R staged candidates; returns
-// (on every lane) the k-th value when there are k, else -inf.
-template <int R>
-__device__ float seg_topk_list(Scratch& sm, int n, int k, uint2* gc, int lane) {
-  unsigned long long key[R];
+// Bitonic sort of one value per lane, descending across the warp.
+__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int i = lane * R + r;
-    key[r] = (i < n) ? sort_key(sm.cand_val[i], sm.cand_idx[i]) : 0ull;
-  }
-  warp_sort_keys_desc<R>(key, lane);
-  float kth = -INFINITY;
+  for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int i = lane * R + r;
-    if (i < n && i < k) gc[i] = make_uint2(static_cast<uint32_t>(skey_idx(key[r])), __float_as_uint(skey_val(key[r])));
-    if (i < n && i == k - 1) kth = skey_val(key[r]);
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(FULL, v, j);
+      const bool desc = (lane & k) == 0, lower = (lane & j) == 0;
+      v = (desc == lower) ? fmaxf(v, o) : fminf(v, o);
+    }
   }
-  return __shfl_sync(FULL, kth, ((k - 1) / R) & 31);
+  return v;
+}
+
+// Entries of the descending list s[0, 32) that are >= v (> v when strict).
+__device__ __forceinline__ int count_at_least(const float* s, float v, bool strict) {
+  int pos = 0;
+#pragma unroll
+  for (int step = 32; step > 0; step >>= 1) {
+    if (pos + step <= 32) {
+      const float x = s[pos + step - 1];
+      if (strict ? (x > v) : (x >= v)) pos += step;
+    }
+  }
+  return pos;
 }
 
 // ---------------------------------------------------------------------------
@@ -1841,13 +1907,31 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 // cuts, records the row and -- for the last row of a sequence to finish, found
 // by a counter -- runs the sequence's accept tests and final draw.
 
+__device__ __forceinline__ int fast_div(int n, uint32_t m, uint32_t s) {
+  return static_cast<int>((__umulhi(static_cast<uint32_t>(n), m) + static_cast<uint32_t>(n)) >> s);
+}
+
+// Source of an item: row = item / nseg, then the row's place (decode_job's
+// mapping) with the divisions done by multiply-high.
 template <typename E>
 __device__ __forceinline__ const E* item_src(const KArgs& a, int item, int* s0, int* L) {
-  const int row = item / a.nseg, seg = item - row * a.nseg;
-  const RowInfo ri = decode_job(a, row);
+  const int row = fast_div(item, a.nseg_m, a.nseg_s);
+  const int seg = item - row * a.nseg;
+  int64_t off;
+  bool tgt;
+  if (a.mode == kModeVerify) {
+    const int b = fast_div(row, a.rows_m, a.rows_s), r = row - b * a.R;
+    tgt = r <= a.K;
+    off = tgt ? static_cast<int64_t>(b) * a.tgt_seq + static_cast<int64_t>(r) * a.tgt_row
+              : static_cast<int64_t>(b) * a.drf_seq + static_cast<int64_t>(r - (a.K + 1)) * a.drf_row;
+  } else {
+    const int b = fast_div(row, a.rows_m, a.rows_s), t = row - b * a.K;
+    tgt = false;
+    off = static_cast<int64_t>(b) * a.drf_seq + static_cast<int64_t>(t) * a.drf_row;
+  }
   *s0 = seg * a.S;
   *L = min(a.S, a.V - *s0);
-  return static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off + *s0;
+  return static_cast<const E*>(tgt ? a.tgt : a.drf) + off + *s0;
 }
 
 // Thread 0: start the bulk copy of an item's 16-byte-aligned part into a
@@ -1886,6 +1970,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
   const int nitems = a.nrows * a.nseg;
   const int grid = static_cast<int>(gridDim.x);
   const int first = static_cast<int>(blockIdx.x);
+  unsigned long long* ckey = reinterpret_cast<unsigned long long*>(sm.cand_idx);  // kSegCap candidate keys
 
   // a bulk copy needs 16-byte-aligned rows; a copy that misses its bounded wait
   // switches the CTA to plain loads (the stray copy is awaited before exit)
@@ -1896,8 +1981,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
     mbar_init(&sm.bar[0], 1);
     mbar_init(&sm.bar[1], 1);
     fence_mbar_init();
-    sm.seg_n = 0;
-    sm.theta = -INFINITY;
+    sm.seg_cnt[0] = sm.seg_cnt[1] = 0;
   }
   __syncthreads();
   if (staged) {
@@ -1926,7 +2010,12 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
       if (lost) { if (p) stray1 = true; else stray0 = true; }
     }
     const bool from_smem = issued && !lost;
-    auto vec = [&](int j) { return item_vec<E>(g, L, from_smem, a.aligned != 0, seg, j * kThreads + tid); };
+    const int nv = L / N;  // vectors wholly inside the item
+    auto vec = [&](int j) -> uint4 {
+      const int v = j * kThreads + tid;
+      if (from_smem && v < nv) return seg[v];
+      return item_vec<E>(g, L, false, a.aligned != 0, seg, v);
+    };
 
     // ---- pass 1: per-vector and per-thread maxima (NaN-propagating)
     float vm[kNV];
@@ -1940,8 +2029,12 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) wm = max_nan(wm, __shfl_xor_sync(FULL, wm, o));
     if (lane == 0) sm.wf[warp] = wm;
-    sm.tmax[tid] = tm;
+    const float srt = a.filt ? warp_sort_desc(tm, lane) : 0.0f;
+    if (a.filt) sm.tmax[tid] = srt;  // each warp's maxima, descending
     if (__syncthreads_or(lost)) staged = false;  // S1
+    // item k counts candidates in seg_cnt[k & 1]; every thread read the other
+    // counter (item k - 1's) before this barrier, so it can be cleared now
+    if (tid == 0) sm.seg_cnt[p ^ 1] = 0;
     float ms = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) ms = max_nan(ms, sm.wf[w]);
@@ -1988,23 +2081,17 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
       if (lane == 0) sm.wd[warp] = wz;
     }
 
-    // ---- candidate floor: the n0-th largest thread maximum.  Each thread ranks
-    // its maximum among all kThreads under (value desc, thread asc); exactly one
-    // thread has rank n0 - 1.
+    // ---- candidate floor: the n0-th largest thread maximum.  Ranks order the
+    // kThreads maxima by (value desc, warp, position in the warp's sorted list):
+    // a thread counts the larger entries of the other warps' lists by binary
+    // search, and exactly one thread has rank n0 - 1.
     const bool cands = a.filt && live && a.n0 <= kThreads;
     if (cands) {
-      int rank = 0;
-      const float4* t4 = reinterpret_cast<const float4*>(sm.tmax);
-#pragma unroll 8
-      for (int q = 0; q < kThreads / 4; ++q) {
-        const float4 v = t4[q];
-        const int u = 4 * q;
-        rank += (v.x > tm || (v.x == tm && u < tid)) ? 1 : 0;
-        rank += (v.y > tm || (v.y == tm && u + 1 < tid)) ? 1 : 0;
-        rank += (v.z > tm || (v.z == tm && u + 2 < tid)) ? 1 : 0;
-        rank += (v.w > tm || (v.w == tm && u + 3 < tid)) ? 1 : 0;
-      }
-      if (rank == a.n0 - 1) sm.theta = tm;
+      int rank = lane;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w)
+        if (w != warp) rank += count_at_least(sm.tmax + w * 32, srt, w > warp);
+      if (rank == a.n0 - 1) sm.theta = srt;
     }
     __syncthreads();  // S2
 
@@ -2024,11 +2111,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
         for (int i = 0; i < N; ++i) {
           const float x = Seg<E>::get(q, i);
           if (x >= theta && x > -INFINITY) {
-            const int pos = atomicAdd(&sm.seg_n, 1);
-            if (pos < kSegCap) {
-              sm.cand_idx[pos] = s0 + (j * kThreads + tid) * N + i;
-              sm.cand_val[pos] = x;
-            }
+            const int pos = atomicAdd(&sm.seg_cnt[p], 1);
+            if (pos < kSegCap) ckey[pos] = sort_key(x, s0 + (j * kThreads + tid) * N + i);
           }
         }
       }
@@ -2044,44 +2128,42 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
       item_issue<E>(a, nxt, bufs + p * a.seg_bytes, &sm.bar[p]);
     }
 
-    // ---- warp 0: the segment's list and record; the other warps go on
-    if (warp == 0) {
-      const int n = sm.seg_n;
-      const bool over = a.filt && live && (!cands || n > kSegCap);
-      const bool use_k = a.top_k > 0;
+    // ---- the segment's list in rank order (value desc, index asc): a
+    // candidate's rank is the number of larger keys; top-k keeps ranks < k.
+    // Its record: thread 0, except the k-th value, which the candidate of rank
+    // k - 1 writes.  No barrier: the keys are rewritten only after the next
+    // item's second barrier.
+    const int n = sm.seg_cnt[p];
+    const bool over = a.filt && live && (!cands || n > kSegCap);
+    const bool use_k = a.top_k > 0;
+    const bool listed = cands && !over;
+    const int keep = use_k ? min(n, a.top_k) : n;
+    SegRec* rec = a.segs + cur;
+    if (listed) {
       uint2* gc = a.seg_cand + static_cast<int64_t>(cur) * kSegCap;
-      float kth = -INFINITY;
-      if (cands && !over) {
-        if (use_k) {
-          if (n <= 64) kth = seg_topk_list<2>(sm, n, a.top_k, gc, lane);
-          else if (n <= 128) kth = seg_topk_list<4>(sm, n, a.top_k, gc, lane);
-          else kth = seg_topk_list<8>(sm, n, a.top_k, gc, lane);
-        } else {
-          for (int c = lane; c < n; c += 32)
-            gc[c] = make_uint2(static_cast<uint32_t>(sm.cand_idx[c]), __float_as_uint(sm.cand_val[c]));
-        }
+      for (int c = tid; c < n; c += kThreads) {
+        const unsigned long long key = ckey[c];
+        int rank = 0;
+#pragma unroll 4
+        for (int q = 0; q < n; ++q) rank += (ckey[q] > key) ? 1 : 0;
+        if (rank < keep) gc[rank] = make_uint2(static_cast<uint32_t>(skey_idx(key)), __float_as_uint(skey_val(key)));
+        if (use_k && rank == a.top_k - 1) rec->kth = skey_val(key);
       }
-      if (lane == 0) {
-        int amin = INT_MAX;
-        for (int w = 0; w < kWarps; ++w) amin = min(amin, sm.wi[w]);
-        FF z = ff(0.0f);
-        if (a.need_z && live)
-          for (int w = 0; w < kWarps; ++w) z = ff_add(z, sm.wd[w]);
-        SegRec r;
-        r.m = ms;
-        r.argmax = (amin == INT_MAX) ? -1 : s0 + amin;
-        r.z_hi = z.hi;
-        r.z_lo = z.lo;
-        r.theta = cands ? theta : -INFINITY;
-        r.kth = (cands && !over && use_k && n >= a.top_k) ? kth : -INFINITY;
-        r.ncand = (cands && !over) ? (use_k ? min(n, a.top_k) : n) : 0;
-        r.flags = (bad ? kSegBad : 0) | (over ? kSegOver : 0);
-        r.off = 0;
-        r.pad_[0] = r.pad_[1] = r.pad_[2] = 0;
-        a.segs[cur] = r;
-        sm.seg_n = 0;  // the next item's candidates (its first barrier orders this)
-        sm.theta = -INFINITY;
-      }
+    }
+    if (tid == 0) {
+      int amin = INT_MAX;
+      for (int w = 0; w < kWarps; ++w) amin = min(amin, sm.wi[w]);
+      FF z = ff(0.0f);
+      if (a.need_z && live)
+        for (int w = 0; w < kWarps; ++w) z = ff_add(z, sm.wd[w]);
+      rec->m = ms;
+      rec->argmax = (amin == INT_MAX) ? -1 : s0 + amin;
+      rec->z_hi = z.hi;
+      rec->z_lo = z.lo;
+      rec->theta = cands ? theta : -INFINITY;
+      if (!(listed && use_k && n >= a.top_k)) rec->kth = -INFINITY;
+      rec->ncand = listed ? keep : 0;
+      rec->flags = (bad ? kSegBad : 0) | (over ? kSegOver : 0);
     }
   }
   // copies that missed their wait must land before the shared memory is released
@@ -2101,7 +2183,6 @@ __global__ void __launch_bounds__(kThreads) spec_row_kernel(const KArgs a) {
   for (int row = static_cast<int>(blockIdx.x); row < a.nrows; row += static_cast<int>(gridDim.x)) {
     const RowInfo ri = decode_job(a, row);
     const E* grow = static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off;
-    row_merge(a, row, sm, sb, pool_idx, pool_val);
     Local C;
     row_finish<E>(a, ri, grow, sm, C, sb, pool_idx, pool_val);
     // every global write of the row is ordered before the sequence counter
@@ -2288,6 +2369,16 @@ spec_status launch(const spec_params* p, const Plan& pl, KArgs& a, DevInfo* di) 
   return SPEC_OK;
 }
 
+// Multiplier and shift for division by d (1 <= d < 2^31) of 0 <= n < 2^31 by
+// a multiply-high: q = (umulhi(n, m) + n) >> s (Granlund and Montgomery,
+// "Division by Invariant Integers using Multiplication", 1994).
+void div_magic(uint32_t d, uint32_t* m, uint32_t* s) {
+  uint32_t sh = 0;
+  while ((uint64_t(1) << sh) < d) ++sh;
+  *m = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << sh) - d)) / d + 1);
+  *s = sh;
+}
+
 void fill_common(const spec_params* p, const Plan& pl, KArgs& a) {
   char* ws = static_cast<char*>(p->workspace);
   a.tickets = reinterpret_cast<unsigned long long*>(ws + pl.off_tickets);
@@ -2302,6 +2393,7 @@ void fill_common(const spec_params* p, const Plan& pl, KArgs& a) {
   a.R = pl.R;
   a.S = pl.S;
   a.nseg = pl.nseg;
+  div_magic(static_cast<uint32_t>(pl.nseg), &a.nseg_m, &a.nseg_s);
   a.seg_bytes = pl.seg_bytes;
   a.nrows = static_cast<int>(pl.nrows);
   a.greedy = p->greedy ? 1 : 0;
@@ -2314,6 +2406,11 @@ void fill_common(const spec_params* p, const Plan& pl, KArgs& a) {
   a.need_z = (!p->greedy && !use_k) ? 1 : 0;
   a.n0 = pl.n0;
   a.status = p->status;
+}
+
+// rows per sequence for the fast division (after a.mode is set)
+void fill_rows_div(KArgs& a) {
+  div_magic(static_cast<uint32_t>(a.mode == kModeVerify ? a.R : a.K), &a.rows_m, &a.rows_s);
 }
 
 bool workspace_ok(const spec_params* p, const Plan& pl) {
@@ -2368,6 +2465,7 @@ spec_status spec_verify(const void* target_logits, const void* draft_logits, con
   a.mode = kModeVerify;
   a.aligned = al ? 1 : 0;
   fill_common(p, pl, a);
+  fill_rows_div(a);
   return launch(p, pl, a, di);
 }
 
@@ -2396,6 +2494,7 @@ spec_status spec_sample_draft(const void* draft_logits, const double* uniforms, 
   a.mode = kModeSample;
   a.aligned = al ? 1 : 0;
   fill_common(p, pl, a);
+  fill_rows_div(a);
   return launch(p, pl, a, di);
 }
 
