@@ -55,6 +55,7 @@ constexpr int kProbes = 8;      // thresholds evaluated per probe pass
 constexpr int kPool = 1024;     // row candidate pool (shared memory), sorted at the row merge
 constexpr int kSegCap = 256;    // candidates one segment may contribute
 constexpr int kListTable = 4096; // listed entries a row merge can index (one byte each)
+constexpr int kRunCap = 128;    // top-k handled by a running set in the segment kernel
 constexpr size_t kCounterArea = 64 * 1024;  // workspace bytes kept zeroed between calls
 constexpr int kNV = 12;         // 16-byte vectors of a segment per thread (24 KB per segment)
 constexpr int kMaxPasses = 40;  // bound on probe passes (16-bit keys need <= 6, 32-bit <= 11)
@@ -350,6 +351,8 @@ struct alignas(128) Scratch {
   float theta, kth;
   int32_t seg_n, last;
   int32_t seg_cnt[2];   // candidates of items k with k & 1 == 0, 1
+  int32_t run_n[2];     // keys in each half of the running top-k set
+  float run_theta[2];   // its k-th value once it holds k keys, else -inf
   // the row being merged
   unsigned long long row_bound;  // largest key a list head left out (0: none)
   FF row_z;
@@ -359,7 +362,7 @@ struct alignas(128) Scratch {
   int32_t bi[kProbes + 8];
   // candidates of the general path; the draft's kept list in the epilogue
   alignas(8) int32_t cand_idx[kCap];  // segment kernel: kSegCap 64-bit candidate keys
-  float cand_val[kCap];
+  alignas(8) float cand_val[kCap];    // segment kernel: the running top-k set, 2 x kRunCap keys
 };
 
 // Sort keys of the row merge (in the consumed segment buffer, after the pool).
@@ -369,6 +372,7 @@ struct SortBuf {
 static_assert(sizeof(Scratch) <= 8192, "shared scratch grew past its budget");
 static_assert(kCap % kThreads == 0 && kPool % kThreads == 0, "lists are split evenly over the threads");
 static_assert(kSegCap * 8 <= kCap * 4, "a segment's candidate keys are staged in cand_idx");
+static_assert(2 * kRunCap * 8 <= kCap * 4, "the running top-k set lives in cand_val");
 static_assert(sizeof(SegRec) % 16 == 0, "segment records are moved as 16-byte words");
 static_assert(sizeof(Slot) % sizeof(uint32_t) == 0, "slots are copied as 32-bit words");
 static_assert(kThreads * sizeof(SegRec) <= kPool * sizeof(unsigned long long),
@@ -986,6 +990,16 @@ __device__ CutResult sort_and_cut(float m, float c, const int32_t* idx, const fl
     block_sort_keys_desc<2>(key, skey);
 #pragma unroll
     for (int r = 0; r < 2; ++r) skey[threadIdx.x * 2 + r] = key[r];
+  } else if (n <= 4 * kThreads) {
+    unsigned long long key[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = threadIdx.x * 4 + r;
+      key[r] = (i < n) ? sort_key(val[i], idx[i]) : 0ull;
+    }
+    block_sort_keys_desc<4>(key, skey);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) skey[threadIdx.x * 4 + r] = key[r];
   } else {
     unsigned long long key[kPool / kThreads];
 #pragma unroll
@@ -1652,12 +1666,13 @@ template <typename E>
 __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scratch& sm, Local& C, SortBuf sb,
                            int32_t* pool_idx, float* pool_val) {
   const int tid = threadIdx.x;
-  // first the pool of every segment list's head: as many entries as the
-  // 256-key register sort holds
+  // first the pool of every segment list's head: as many entries as a 256-key
+  // (top-k) or 512-key (top-p: the nucleus may be long) register sort holds
   const int row = ri.job;
   const int ns = a.nseg;
-  int lim = (a.top_k > 0) ? min(a.top_k, max(4, 256 / ns)) : max(4, 256 / ns);
-  if (lim >= kSegCap) lim = INT_MAX;
+  int lim = (a.top_k > 0) ? min(a.top_k, max(4, 256 / ns)) : max(4, 512 / ns);
+  // top-k through a running set: a few lists of k keys each, taken whole
+  if (lim >= kSegCap || (a.top_k > 0 && a.top_k <= kRunCap)) lim = INT_MAX;
   row_merge(a, row, sm, sb, pool_idx, pool_val, lim, -INFINITY);
   const float m = sm.row_m;
   const int argmax = sm.row_argmax;
@@ -1968,9 +1983,15 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
   constexpr int N = Seg<E>::N;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nitems = a.nrows * a.nseg;
-  const int grid = static_cast<int>(gridDim.x);
-  const int first = static_cast<int>(blockIdx.x);
-  unsigned long long* ckey = reinterpret_cast<unsigned long long*>(sm.cand_idx);  // kSegCap candidate keys
+  // this CTA's items: one contiguous range, so it meets a row's segments in order
+  const int beg = static_cast<int>(static_cast<int64_t>(blockIdx.x) * nitems / gridDim.x);
+  const int end = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * nitems / gridDim.x);
+  unsigned long long* ckey = reinterpret_cast<unsigned long long*>(sm.cand_idx);  // an item's candidate keys
+  unsigned long long* run = reinterpret_cast<unsigned long long*>(sm.cand_val);   // two halves of kRunCap keys
+  // top-k with a running set: the CTA keeps the top k keys of the row segments
+  // it has met so far; once it holds k, its k-th value is a floor for the row's
+  // k-th value, and later segments of the row only collect elements >= it
+  const bool stream_k = a.filt && a.top_k > 0 && a.top_k <= kRunCap;
 
   // a bulk copy needs 16-byte-aligned rows; a copy that misses its bounded wait
   // switches the CTA to plain loads (the stray copy is awaited before exit)
@@ -1982,20 +2003,26 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
     mbar_init(&sm.bar[1], 1);
     fence_mbar_init();
     sm.seg_cnt[0] = sm.seg_cnt[1] = 0;
+    sm.run_n[0] = sm.run_n[1] = 0;
+    sm.run_theta[0] = sm.run_theta[1] = -INFINITY;
   }
   __syncthreads();
   if (staged) {
-    issued0 = first < nitems;
-    issued1 = first + grid < nitems;
+    issued0 = beg < end;
+    issued1 = beg + 1 < end;
     if (tid == 0) {
-      if (issued0) item_issue<E>(a, first, bufs, &sm.bar[0]);
-      if (issued1) item_issue<E>(a, first + grid, bufs + a.seg_bytes, &sm.bar[1]);
+      if (issued0) item_issue<E>(a, beg, bufs, &sm.bar[0]);
+      if (issued1) item_issue<E>(a, beg + 1, bufs + a.seg_bytes, &sm.bar[1]);
     }
   }
 
-  int k = 0;
-  for (int cur = first; cur < nitems; cur += grid, ++k) {
+  int k = 0, rp = 0, prev_row = -1;  // rp: the half of run[] holding the running set
+  for (int cur = beg; cur < end; ++cur, ++k) {
     const int p = k & 1;
+    const int row = fast_div(cur, a.nseg_m, a.nseg_s);
+    const bool new_run = row != prev_row;
+    prev_row = row;
+    const bool run_ends = cur + 1 >= end || fast_div(cur + 1, a.nseg_m, a.nseg_s) != row;
     int s0, L;
     const E* g = item_src<E>(a, cur, &s0, &L);
     const uint4* seg = reinterpret_cast<const uint4*>(bufs + p * a.seg_bytes);
@@ -2016,8 +2043,12 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
       if (from_smem && v < nv) return seg[v];
       return item_vec<E>(g, L, false, a.aligned != 0, seg, v);
     };
+    // the running floor, when the set already holds k keys of this row
+    const float rfloor = (stream_k && !new_run) ? sm.run_theta[rp] : -INFINITY;
+    const bool steady = rfloor > -INFINITY;
 
-    // ---- pass 1: per-vector and per-thread maxima (NaN-propagating)
+    // ---- pass 1: per-vector and per-thread maxima (NaN-propagating); with a
+    // running floor, the elements >= it are collected in the same pass
     float vm[kNV];
     float tm = -INFINITY;
 #pragma unroll
@@ -2025,12 +2056,32 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
       vm[j] = Seg<E>::vmax(vec(j));
       tm = max_nan(tm, vm[j]);
     }
+    if (steady && tm >= rfloor) {
+      uint32_t mask = 0;
+#pragma unroll
+      for (int j = 0; j < kNV; ++j)
+        if (vm[j] >= rfloor) mask |= 1u << j;
+      while (mask) {
+        const int j = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const uint4 q = vec(j);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+          const float x = Seg<E>::get(q, i);
+          if (x >= rfloor) {
+            const int pos = atomicAdd(&sm.seg_cnt[p], 1);
+            if (pos < kSegCap) ckey[pos] = sort_key(x, s0 + (j * kThreads + tid) * N + i);
+          }
+        }
+      }
+    }
     float wm = tm;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) wm = max_nan(wm, __shfl_xor_sync(FULL, wm, o));
     if (lane == 0) sm.wf[warp] = wm;
-    const float srt = a.filt ? warp_sort_desc(tm, lane) : 0.0f;
-    if (a.filt) sm.tmax[tid] = srt;  // each warp's maxima, descending
+    const float srt = (a.filt && !steady) ? warp_sort_desc(tm, lane) : 0.0f;
+    if (a.filt && !steady) sm.tmax[tid] = srt;  // each warp's maxima, descending
+    if (tid == 0) sm.run_theta[rp ^ 1] = -INFINITY;  // set by this item's merge when it holds k keys
     if (__syncthreads_or(lost)) staged = false;  // S1
     // item k counts candidates in seg_cnt[k & 1]; every thread read the other
     // counter (item k - 1's) before this barrier, so it can be cleared now
@@ -2081,66 +2132,95 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
       if (lane == 0) sm.wd[warp] = wz;
     }
 
-    // ---- candidate floor: the n0-th largest thread maximum.  Ranks order the
-    // kThreads maxima by (value desc, warp, position in the warp's sorted list):
-    // a thread counts the larger entries of the other warps' lists by binary
-    // search, and exactly one thread has rank n0 - 1.
-    const bool cands = a.filt && live && a.n0 <= kThreads;
-    if (cands) {
-      int rank = lane;
+    // ---- without a running floor: the candidate floor is the n0-th largest
+    // thread maximum.  Ranks order the kThreads maxima by (value desc, warp,
+    // position in the warp's sorted list); exactly one thread has rank n0 - 1.
+    const bool cands = a.filt && live && a.n0 <= kThreads && !steady;
+    float theta = rfloor;
+    if (a.filt && !steady) {
+      if (cands) {
+        int rank = lane;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w)
-        if (w != warp) rank += count_at_least(sm.tmax + w * 32, srt, w > warp);
-      if (rank == a.n0 - 1) sm.theta = srt;
-    }
-    __syncthreads();  // S2
-
-    // ---- candidates: every finite element >= theta, from the vectors whose
-    // maximum reaches it, staged in the candidate arrays
-    const float theta = sm.theta;
-    if (cands && tm >= theta) {
-      uint32_t mask = 0;
+        for (int w = 0; w < kWarps; ++w)
+          if (w != warp) rank += count_at_least(sm.tmax + w * 32, srt, w > warp);
+        if (rank == a.n0 - 1) sm.theta = srt;
+      }
+      __syncthreads();  // S2
+      theta = sm.theta;
+      // every finite element >= theta, from the vectors whose maximum reaches it
+      if (cands && tm >= theta) {
+        uint32_t mask = 0;
 #pragma unroll
-      for (int j = 0; j < kNV; ++j)
-        if (vm[j] >= theta) mask |= 1u << j;
-      while (mask) {
-        const int j = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const uint4 q = vec(j);
+        for (int j = 0; j < kNV; ++j)
+          if (vm[j] >= theta) mask |= 1u << j;
+        while (mask) {
+          const int j = __ffs(mask) - 1;
+          mask &= mask - 1;
+          const uint4 q = vec(j);
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-          const float x = Seg<E>::get(q, i);
-          if (x >= theta && x > -INFINITY) {
-            const int pos = atomicAdd(&sm.seg_cnt[p], 1);
-            if (pos < kSegCap) ckey[pos] = sort_key(x, s0 + (j * kThreads + tid) * N + i);
+          for (int i = 0; i < N; ++i) {
+            const float x = Seg<E>::get(q, i);
+            if (x >= theta && x > -INFINITY) {
+              const int pos = atomicAdd(&sm.seg_cnt[p], 1);
+              if (pos < kSegCap) ckey[pos] = sort_key(x, s0 + (j * kThreads + tid) * N + i);
+            }
           }
         }
       }
+      __syncthreads();  // S3: the candidates are complete
     }
-    __syncthreads();  // S3: the buffer and the candidates are complete
-
-    // ---- refill the buffer with the item two ahead
-    const int nxt = cur + 2 * grid;
-    const bool refill = staged && nxt < nitems;
-    if (p) issued1 = refill; else issued0 = refill;
-    if (tid == 0 && refill) {
-      fence_proxy_async_smem();
-      item_issue<E>(a, nxt, bufs + p * a.seg_bytes, &sm.bar[p]);
-    }
-
-    // ---- the segment's list in rank order (value desc, index asc): a
-    // candidate's rank is the number of larger keys; top-k keeps ranks < k.
-    // Its record: thread 0, except the k-th value, which the candidate of rank
-    // k - 1 writes.  No barrier: the keys are rewritten only after the next
-    // item's second barrier.
     const int n = sm.seg_cnt[p];
-    const bool over = a.filt && live && (!cands || n > kSegCap);
-    const bool use_k = a.top_k > 0;
-    const bool listed = cands && !over;
-    const int keep = use_k ? min(n, a.top_k) : n;
+    const bool collected = cands || (steady && live);
+    const bool over = a.filt && live && (!collected || n > kSegCap);
+    const bool listed = collected && !over;
     SegRec* rec = a.segs + cur;
-    if (listed) {
-      uint2* gc = a.seg_cand + static_cast<int64_t>(cur) * kSegCap;
+    uint2* gc = a.seg_cand + static_cast<int64_t>(cur) * kSegCap;
+    int ncand = 0;
+    float kth = -INFINITY;
+
+    if (stream_k) {
+      // ---- merge the new keys into the running set (sorted desc, at most k):
+      // a key's new position is the number of larger keys in both lists
+      const int rn = new_run ? 0 : sm.run_n[rp];
+      const unsigned long long* src = run + rp * kRunCap;
+      unsigned long long* dst = run + (rp ^ 1) * kRunCap;
+      const int nn = listed ? n : 0;
+      const int K = a.top_k;
+      for (int i = tid; i < rn; i += kThreads) {
+        const unsigned long long key = src[i];
+        int r = i;
+        for (int c = 0; c < nn; ++c) r += (ckey[c] > key) ? 1 : 0;
+        if (r < K) dst[r] = key;
+        if (r == K - 1) sm.run_theta[rp ^ 1] = skey_val(key);
+      }
+      for (int c = tid; c < nn; c += kThreads) {
+        const unsigned long long key = ckey[c];
+        int lo = 0, hi = rn;  // larger keys of the sorted running set
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (src[mid] > key) lo = mid + 1; else hi = mid;
+        }
+        int r = lo;
+        for (int q = 0; q < nn; ++q) r += (ckey[q] > key) ? 1 : 0;
+        if (r < K) dst[r] = key;
+        if (r == K - 1) sm.run_theta[rp ^ 1] = skey_val(key);
+      }
+      const int new_n = min(K, rn + nn);
+      if (tid == 0) sm.run_n[rp ^ 1] = new_n;
+      __syncthreads();  // the merged set (and the buffer's last reads) are complete
+      rp ^= 1;
+      // the run ends here: its top k is the list of this item
+      if (run_ends && !over) {
+        for (int i = tid; i < new_n; i += kThreads)
+          gc[i] = make_uint2(static_cast<uint32_t>(skey_idx(dst[i])), __float_as_uint(skey_val(dst[i])));
+        ncand = new_n;
+        kth = (new_n >= K) ? sm.run_theta[rp] : -INFINITY;
+      }
+    } else if (listed) {
+      // ---- per-item list in rank order (value desc, index asc): top-k keeps
+      // ranks < k, and the candidate of rank k - 1 is the k-th value
+      const bool use_k = a.top_k > 0;
+      const int keep = use_k ? min(n, a.top_k) : n;
       for (int c = tid; c < n; c += kThreads) {
         const unsigned long long key = ckey[c];
         int rank = 0;
@@ -2149,7 +2229,22 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
         if (rank < keep) gc[rank] = make_uint2(static_cast<uint32_t>(skey_idx(key)), __float_as_uint(skey_val(key)));
         if (use_k && rank == a.top_k - 1) rec->kth = skey_val(key);
       }
+      ncand = keep;
     }
+
+    // ---- refill the buffer with the item two ahead, once every read of it is
+    // done: the merge barrier (running top-k) or S3 (other filters) followed
+    // them; without a filter the argmax and normaliser passes need one here
+    if (!a.filt) __syncthreads();
+    const int nxt = cur + 2;
+    const bool refill = staged && nxt < end;
+    if (p) issued1 = refill; else issued0 = refill;
+    if (tid == 0 && refill) {
+      fence_proxy_async_smem();
+      item_issue<E>(a, nxt, bufs + p * a.seg_bytes, &sm.bar[p]);
+    }
+
+    // ---- the segment record (thread 0)
     if (tid == 0) {
       int amin = INT_MAX;
       for (int w = 0; w < kWarps; ++w) amin = min(amin, sm.wi[w]);
@@ -2160,15 +2255,19 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
       rec->argmax = (amin == INT_MAX) ? -1 : s0 + amin;
       rec->z_hi = z.hi;
       rec->z_lo = z.lo;
-      rec->theta = cands ? theta : -INFINITY;
-      if (!(listed && use_k && n >= a.top_k)) rec->kth = -INFINITY;
-      rec->ncand = listed ? keep : 0;
+      rec->theta = collected ? theta : -INFINITY;
+      if (stream_k) rec->kth = kth;
+      else if (!(listed && a.top_k > 0 && n >= a.top_k)) rec->kth = -INFINITY;
+      rec->ncand = ncand;
       rec->flags = (bad ? kSegBad : 0) | (over ? kSegOver : 0);
     }
   }
   // copies that missed their wait must land before the shared memory is released
   if (stray0) (void)mbar_wait_bounded(&sm.bar[0], ph0 ^ 1u);
   if (stray1) (void)mbar_wait_bounded(&sm.bar[1], ph1 ^ 1u);
+  // this CTA is done: the row kernel may be scheduled (it still waits for the
+  // whole grid's memory before reading it)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Row merge, cut, record and (verify) the sequence counter and epilogue.
@@ -2180,6 +2279,9 @@ __global__ void __launch_bounds__(kThreads) spec_row_kernel(const KArgs a) {
   int32_t* pool_idx = reinterpret_cast<int32_t*>(scratch);
   float* pool_val = reinterpret_cast<float*>(pool_idx + kPool);
   const SortBuf sb{reinterpret_cast<unsigned long long*>(pool_val + kPool)};
+  // launched as a programmatic dependent of the segment kernel: wait until that
+  // grid has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int row = static_cast<int>(blockIdx.x); row < a.nrows; row += static_cast<int>(gridDim.x)) {
     const RowInfo ri = decode_job(a, row);
     const E* grow = static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off;
@@ -2357,14 +2459,27 @@ spec_status launch(const spec_params* p, const Plan& pl, KArgs& a, DevInfo* di) 
   cudaStream_t st = static_cast<cudaStream_t>(p->stream);
   if (pl.clear_counters && cudaMemsetAsync(p->workspace, 0, pl.counter_bytes, st) != cudaSuccess)
     return SPEC_ERR_CUDA;
+  // the row kernel is a programmatic dependent launch: it may be scheduled
+  // while the segment kernel's last CTAs finish, and waits in its prologue
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = rgrid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = pl.row_smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (p->dtype == SPEC_F32) {
     spec_seg_kernel<float><<<grid, block, pl.smem, st>>>(a);
-    spec_row_kernel<float><<<rgrid, block, pl.row_smem, st>>>(a);
+    e = cudaLaunchKernelEx(&cfg, spec_row_kernel<float>, a);
   } else {
     spec_seg_kernel<uint16_t><<<grid, block, pl.smem, st>>>(a);
-    spec_row_kernel<uint16_t><<<rgrid, block, pl.row_smem, st>>>(a);
+    e = cudaLaunchKernelEx(&cfg, spec_row_kernel<uint16_t>, a);
   }
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   g_launches.fetch_add(2, std::memory_order_relaxed);
   return SPEC_OK;
 }
