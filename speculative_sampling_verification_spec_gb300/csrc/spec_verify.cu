@@ -361,7 +361,7 @@ struct alignas(128) Scratch {
   FF bd[kProbes + 4];
   int32_t bi[kProbes + 8];
   // candidates of the general path; the draft's kept list in the epilogue
-  alignas(8) int32_t cand_idx[kCap];  // segment kernel: kSegCap 64-bit candidate keys
+  alignas(16) int32_t cand_idx[kCap];  // segment kernel: kSegCap 64-bit candidate keys
   alignas(8) float cand_val[kCap];    // segment kernel: the running top-k set, 2 x kRunCap keys
 };
 
@@ -1298,14 +1298,13 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
   const spec_row_stat* recs = a.rows + static_cast<int64_t>(b) * R;
   int32_t* out = a.out_tokens + static_cast<int64_t>(b) * (K + 1);
   const int tid = threadIdx.x;
-  // all row records in parallel: flags, then the first rejection (one test per thread)
+  // all row records in parallel, in one round of loads: the flags, and the
+  // accept tests (one per thread; the flags decide afterwards whether they count)
   if (tid == 0) { sm.bi[12] = 0; sm.bi[13] = K; }
   __syncthreads();
   int myfl = 0;
   for (int r = tid; r < R; r += kThreads) myfl |= __ldcg(&recs[r].flags);
-  if (myfl) atomicOr(&sm.bi[12], myfl);
-  __syncthreads();
-  if (sm.bi[12] == 0) {
+  {
     for (int t = tid; t < K; t += kThreads) {
       const int d = a.tokens[static_cast<int64_t>(b) * K + t];
       bool acc;
@@ -1320,6 +1319,7 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
       if (!acc) atomicMin(&sm.bi[13], t);  // the first rejection wins
     }
   }
+  if (myfl) atomicOr(&sm.bi[12], myfl);
   __syncthreads();
   const int fl = sm.bi[12], n = sm.bi[13];
   __syncthreads();
@@ -1510,15 +1510,38 @@ __device__ void general_cut(const KArgs& a, const RowCtx<E>& rg, Scratch& sm, Lo
 // position is the number of kept entries with a smaller index.
 __device__ void write_kept_by_index(const unsigned long long* skey, int n, float m, float c, int32_t* lidx,
                                     float* lw, Scratch& sm) {
-  int32_t* kidx = sm.cand_idx;  // the indices, unpacked once
+  constexpr int G = kCap / kThreads;  // entries per thread: threadIdx.x + g * kThreads
+  int32_t* kidx = sm.cand_idx;        // the indices, unpacked once
   for (int i = threadIdx.x; i < n; i += kThreads) kidx[i] = skey_idx(skey[i]);
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += kThreads) {
-    const int xi = kidx[i];
-    int pos = 0;
-    for (int j = 0; j < n; ++j) pos += (kidx[j] < xi) ? 1 : 0;
-    lidx[pos] = xi;
-    lw[pos] = wexp(skey_val(skey[i]), m, c);
+  // each thread ranks all its entries in one pass over the indices, four at a time
+  int xi[G], pos[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int i = threadIdx.x + g * kThreads;
+    xi[g] = (i < n) ? kidx[i] : INT_MIN;
+    pos[g] = 0;
+  }
+  const int4* k4 = reinterpret_cast<const int4*>(kidx);
+  const int n4 = n >> 2;
+  for (int j = 0; j < n4; ++j) {
+    const int4 v = k4[j];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      pos[g] += (v.x < xi[g]) + (v.y < xi[g]) + (v.z < xi[g]) + (v.w < xi[g]);
+  }
+  for (int j = n4 << 2; j < n; ++j) {
+    const int v = kidx[j];
+#pragma unroll
+    for (int g = 0; g < G; ++g) pos[g] += (v < xi[g]) ? 1 : 0;
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int i = threadIdx.x + g * kThreads;
+    if (i < n) {
+      lidx[pos[g]] = xi[g];
+      lw[pos[g]] = wexp(skey_val(skey[i]), m, c);
+    }
   }
   __syncthreads();
 }
