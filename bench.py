@@ -375,6 +375,21 @@ def run_gpu(args, name):
         e2e_s = float(t.item())
     e2e_val = world * rows_step * e2e_steps / e2e_s
 
+    # acceptance telemetry on the last verify's counts (outside the timed step):
+    # launch latency, as it reads only B int32
+    hist = torch.zeros((K + 2,), dtype=torch.int32, device=dev)
+    for _ in range(3):
+        sv.spec_accept_histogram(out_n, K, hist=hist)
+    nh = 200
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    for _ in range(nh):
+        sv.spec_accept_histogram(out_n, K, hist=hist)
+    h1.record(stream)
+    torch.cuda.synchronize(dev)
+    hist_us = h0.elapsed_time(h1) * 1e3 / nh
+    hist_ok = int(hist.sum().item()) == B * (nh + 3)
+
     base_cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base_cpu = cpu_baseline(host_first, os.cpu_count() or 1)
@@ -396,7 +411,11 @@ def run_gpu(args, name):
                                         "gbs": achieved, "rows_per_s": rv / (avg_v / 1e3)},
                         "spec_sample_draft": {"avg_us": avg_s * 1e3, "rows": rs, "bytes": bytes_s,
                                               "gbs": bytes_s / (avg_s / 1e3) / 1e9,
-                                              "rows_per_s": rs / (avg_s / 1e3)}},
+                                              "rows_per_s": rs / (avg_s / 1e3)},
+                        "spec_accept_histogram": {"avg_us": hist_us, "sequences": B, "counts_ok": hist_ok,
+                                                  "accepted_per_round": float(
+                                                      (torch.arange(K + 1, device=dev) * hist[:K + 1]).sum().item()
+                                                      / max(1, int(hist[:K + 1].sum().item())))}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
                          "kernel": "spec_seg_kernel + spec_row_kernel (one spec_verify call)",
@@ -417,6 +436,88 @@ def run_gpu(args, name):
     return 0
 
 
+def run_decode(args):
+    """Decode rounds through the driver (spec_sample_draft x K, then spec_verify)
+    on a source with acceptance exactly 0.8 at the c5 shape: tokens per round
+    against the closed form, and the round rate."""
+    import torch
+    from speculative_sampling_verification_spec_gb300 import decode
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    alpha, B, K, V, rounds = 0.8, 32, 8, 256000, max(10, args.steps // 50)
+    src = workloads.synthetic_source(V=V, S=64, alpha=alpha, seed=12, dtype="bf16")
+    conv = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    tt, dt = conv(src.target), conv(src.draft)
+    first = torch.from_numpy(np.random.default_rng(4).integers(0, V // 2, B)).to(dev)
+    state = lambda last, pos: workloads.state_of(last, pos, src.S)
+    unis = [workloads.round_uniforms(13, r, B, K) for r in range(rounds + 3)]
+    decode.decode_rounds(tt, dt, state, first, K, 3, lambda r: unis[r])
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    got = decode.decode_rounds(tt, dt, state, first, K, rounds, lambda r: unis[r])
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    n1 = torch.cat([n for _, n in got]).double() + 1
+    line = {"mode": "decode", "metric": "tokens per round and rounds/s of the decode loop", "B": B, "K": K, "V": V,
+            "dtype": "bf16", "alpha": alpha, "rounds": rounds,
+            "tokens_per_round": float(n1.mean()), "tokens_per_round_sd": float(n1.std()),
+            "closed_form": decode.expected_tokens_per_round(alpha, K),
+            "ms_per_round": ms / rounds, "rounds_per_s": rounds / (ms / 1e3),
+            "tokens_per_s": float(n1.sum()) / (ms / 1e3),
+            "round": "K spec_sample_draft calls (B rows each) + row gathers standing in for the model calls "
+                     "+ one spec_verify; uniforms copied from the host each round"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sweep_k(args):
+    """spec_verify time against K at the c5 shape (B=32, V=256000 bf16, top-k 50),
+    and the speed-up the latency model gives with that cost added to the pages'
+    round (Chinchilla 70B target 14.1 ms per call, 4B draft 1.8 ms per call)."""
+    import torch
+    import speculative_sampling_verification_spec_gb300 as sv
+    from speculative_sampling_verification_spec_gb300 import decode
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    t_target, t_draft = 14.1, 1.8
+    c = t_draft / t_target
+    rows = []
+    for K in range(1, 9):
+        w = workloads.make("c5", K=K)
+        prm = dict(temperature=w["temperature"], top_k=w["top_k"], top_p=w["top_p"], greedy=w["greedy"])
+        conv = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        tgt, drf = conv(w["target"]), conv(w["draft"])
+        tok = sv.spec_sample_draft(drf, torch.from_numpy(w["u_draft"]).to(dev), **prm)
+        uv = torch.from_numpy(w["u_verify"]).to(dev)
+        for _ in range(5):
+            sv.spec_verify(tgt, drf, tok, uv, **prm)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 50
+        e0.record()
+        for _ in range(n):
+            sv.spec_verify(tgt, drf, tok, uv, **prm)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) * 1e3 / n
+        rows.append({"K": K, "verify_us": us, "rows": w["B"] * (2 * K + 1)})
+    vc = {r["K"]: r["verify_us"] / 1e3 / t_target for r in rows}
+    model = []
+    for alpha in (0.75, 0.8):
+        model.append({"alpha": alpha, "c": c,
+                      "speedup": {r["K"]: decode.speedup(alpha, r["K"], c, vc[r["K"]]) for r in rows},
+                      "speedup_without_verify": {r["K"]: decode.speedup(alpha, r["K"], c) for r in rows},
+                      "best_k": decode.best_k(alpha, c, lambda k: vc.get(k, vc[8]), 8),
+                      "best_k_without_verify": decode.best_k(alpha, c, lambda k: 0.0, 8)})
+    line = {"mode": "sweep_k", "metric": "spec_verify time vs K (c5 shape) and modelled speed-up",
+            "workload": "c5 with K = 1..8 (B=32, V=256000 bf16, top_k=50)", "verify": rows,
+            "model": model, "t_target_ms": t_target, "t_draft_ms": t_draft}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,9 +526,15 @@ def main():
     ap.add_argument("--workload", default="c5", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true", help="decode-loop line instead of the verify line")
+    ap.add_argument("--sweep-k", action="store_true", help="verify time vs K and the latency model")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.decode:
+        return run_decode(args)
+    if args.sweep_k:
+        return run_sweep_k(args)
     if args.impl == "reference":
         return run_reference(args, args.workload)
     return run_gpu(args, args.workload)

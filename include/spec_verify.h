@@ -204,6 +204,25 @@ const char* spec_status_string(spec_status status);
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t spec_launch_count(void);
 
+/* Acceptance telemetry: adds the histogram of one call's accepted-draft counts
+ * to hist.  The share of draft tokens accepted per round is the quantity to
+ * watch ("Speculative decoding: how to run large models faster", ai-trend.me,
+ * section "Limitations and open issues": fewer accepted tokens per round
+ * means more target work), and out_num_accepted carries it per sequence.
+ *   out_num_accepted  device int32 [B], as written by spec_verify
+ *   B                 sequences (>= 0; 0 launches nothing)
+ *   K                 draft tokens per sequence, 1 <= K <= 8192
+ *   hist              device int32 [K+2], caller-owned and caller-zeroed:
+ *                     hist[j] += sequences with j accepted tokens (0 <= j <= K),
+ *                     hist[K+1] += sequences that ended in an error (-1) or
+ *                     hold any other value
+ *   stream            cudaStream_t (NULL = default stream)
+ * Asynchronous on stream (one kernel); repeated calls accumulate.
+ * Returns SPEC_ERR_INVALID_ARG (nothing launched) for B < 0, K outside
+ * [1, 8192] or a NULL pointer with B > 0; SPEC_ERR_CUDA if the launch fails. */
+spec_status spec_accept_histogram(const int32_t* out_num_accepted, int32_t B, int32_t K, int32_t* hist,
+                                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,8 @@ def lib():
             L.oracle_sample_draft.argtypes = [P, P, ctypes.POINTER(Params), P, P]
             for f in (L.oracle_row_probs, L.oracle_verify, L.oracle_sample_draft):
                 f.restype = ctypes.c_int
+            L.oracle_accept_histogram.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P]
+            L.oracle_accept_histogram.restype = None
             _lib = L
     return _lib
 
@@ -149,6 +151,17 @@ def sample_draft(draft, uniforms, temperature=1.0, top_k=0, top_p=1.0, greedy=Fa
     u = None if uniforms is None else np.ascontiguousarray(uniforms, dtype=np.float64)
     s = lib().oracle_sample_draft(_ptr(draft), _ptr(u), ctypes.byref(p), _ptr(out_t), _ptr(flags))
     return dict(tokens=out_t, flags=flags, status=s)
+
+
+def accept_histogram(num_accepted, K):
+    """int64 [K+2]: sequences per number of accepted draft tokens 0..K, then the
+    sequences that ended in an error (oracle_accept_histogram in oracle.h)."""
+    n = np.ascontiguousarray(num_accepted, dtype=np.int32)
+    hist = np.zeros(int(K) + 2, dtype=np.int64)
+    L = lib()
+    L.oracle_accept_histogram(n.ctypes.data_as(ctypes.c_void_p), ctypes.c_int64(n.size), ctypes.c_int32(int(K)),
+                              hist.ctypes.data_as(ctypes.c_void_p))
+    return hist
 
 
 def verify_threaded(target, draft, tokens, uniforms, threads, **kw):

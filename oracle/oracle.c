@@ -312,3 +312,16 @@ int oracle_sample_draft(const void* drf, const double* u, const oracle_params* p
   free(P);
   return first_err;
 }
+
+/* Acceptance telemetry: count the sequences per number of accepted draft
+ * tokens; anything outside [0, K] (an error) goes to the last bin. */
+void oracle_accept_histogram(const int32_t* num_accepted, int64_t B, int32_t K, int64_t* hist) {
+  for (int32_t j = 0; j < K + 2; ++j) hist[j] = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    const int32_t n = num_accepted[b];
+    if (n >= 0 && n <= K)
+      hist[n] += 1;
+    else
+      hist[K + 1] += 1;
+  }
+}

@@ -108,6 +108,14 @@ int oracle_verify(const void* tgt, const void* drf, const int32_t* tokens, const
 int oracle_sample_draft(const void* drf, const double* u, const oracle_params* p,
                         int32_t* out_tokens, int32_t* out_flags);
 
+/* Acceptance telemetry: hist[j] = number of sequences b with
+ * num_accepted[b] == j for j in [0, K]; hist[K+1] = the rest (sequences that
+ * ended in an error, num_accepted = -1).  hist has K+2 entries and is
+ * overwritten.  ("Speculative decoding: how to run large models faster",
+ * section "Limitations and open issues": the share of draft tokens accepted
+ * per round is the quantity to watch.) */
+void oracle_accept_histogram(const int32_t* num_accepted, int64_t B, int32_t K, int64_t* hist);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_CUDA", 3: 
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
 EXPORTED = ("spec_verify", "spec_sample_draft", "spec_verify_workspace_size",
             "spec_sample_draft_workspace_size", "spec_read_row_stats", "spec_status_string",
-            "spec_launch_count", "spec_verify_noalloc")
+            "spec_launch_count", "spec_verify_noalloc", "spec_accept_histogram")
 
 
 class SpecParams(ctypes.Structure):
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.spec_status_string.restype = ctypes.c_char_p
             L.spec_verify_noalloc.argtypes = [P, P, P, P, PP, P, P]
             L.spec_verify_noalloc.restype = ctypes.c_int
+            L.spec_accept_histogram.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
+            L.spec_accept_histogram.restype = ctypes.c_int
             L.spec_launch_count.argtypes = []
             L.spec_launch_count.restype = ctypes.c_uint64
             _lib = L
@@ -254,3 +256,22 @@ def spec_verify_noalloc(target, draft, draft_tokens, uniforms, *, temperature=1.
     if code != SPEC_OK:
         raise SpecError(code, "spec_verify_noalloc")
     return out_tokens, out_num_accepted
+
+
+def spec_accept_histogram(out_num_accepted, K, *, hist=None, stream=None):
+    """Add the histogram of accepted-draft counts (out_num_accepted [B] int32 CUDA)
+    to hist (int32 [K+2] CUDA; a zeroed one is made when None): bins 0..K count
+    sequences by accepted tokens, bin K+1 the sequences that ended in an error.
+    Returns hist."""
+    _check_cuda(out_num_accepted)
+    n = out_num_accepted if out_num_accepted.dtype == torch.int32 else out_num_accepted.to(torch.int32)
+    n = n.contiguous()
+    if hist is None:
+        hist = torch.zeros((int(K) + 2,), dtype=torch.int32, device=n.device)
+    _check_cuda(hist)
+    if hist.dtype != torch.int32 or hist.numel() != int(K) + 2 or not hist.is_contiguous():
+        raise ValueError("hist must be a contiguous int32 tensor of K + 2 entries")
+    code = lib().spec_accept_histogram(_ptr(n), int(n.numel()), int(K), _ptr(hist), _stream_handle(stream))
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_accept_histogram")
+    return hist

@@ -58,6 +58,7 @@ constexpr int kListTable = 4096; // listed entries a row merge can index (one by
 constexpr int kRunCap = 128;    // top-k handled by a running set in the segment kernel
 constexpr size_t kCounterArea = 64 * 1024;  // workspace bytes kept zeroed between calls
 constexpr int kNV = 12;         // 16-byte vectors of a segment per thread (24 KB per segment)
+constexpr int kHistMaxK = 8192;  // acceptance histogram: K + 2 bins in shared memory
 constexpr int kMaxPasses = 40;  // bound on probe passes (16-bit keys need <= 6, 32-bit <= 11)
 constexpr unsigned FULL = 0xffffffffu;
 
@@ -2332,6 +2333,26 @@ __global__ void __launch_bounds__(kThreads) spec_row_kernel(const KArgs a) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Acceptance telemetry: a histogram of the accepted-draft counts of a call.
+// Bins 0..K count the sequences by accepted tokens; bin K+1 the sequences that
+// ended in an error.  Each CTA counts in shared memory, then adds its nonzero
+// bins to the caller's histogram.
+
+__global__ void __launch_bounds__(256) spec_hist_kernel(const int32_t* __restrict__ n_acc, int B, int K,
+                                                        int32_t* __restrict__ hist) {
+  extern __shared__ int32_t bins[];
+  for (int i = threadIdx.x; i < K + 2; i += blockDim.x) bins[i] = 0;
+  __syncthreads();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B; i += gridDim.x * blockDim.x) {
+    const int v = __ldg(&n_acc[i]);
+    atomicAdd(&bins[(v >= 0 && v <= K) ? v : K + 1], 1);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < K + 2; i += blockDim.x)
+    if (bins[i] != 0) atomicAdd(&hist[i], bins[i]);
+}
+
 // ===========================================================================
 // host side
 
@@ -2667,6 +2688,23 @@ const char* spec_status_string(spec_status status) {
 }
 
 uint64_t spec_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+spec_status spec_accept_histogram(const int32_t* out_num_accepted, int32_t B, int32_t K, int32_t* hist,
+                                  void* stream) {
+  if (B < 0 || K < 1 || K > kHistMaxK) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!out_num_accepted || !hist) return SPEC_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  const int blocks = static_cast<int>(std::min<int64_t>((static_cast<int64_t>(B) + 255) / 256, 2 * sms));
+  const size_t smem = static_cast<size_t>(K + 2) * sizeof(int32_t);
+  spec_hist_kernel<<<blocks, 256, smem, static_cast<cudaStream_t>(stream)>>>(out_num_accepted, B, K, hist);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return SPEC_OK;
+}
 
 }  // extern "C"
 

@@ -92,3 +92,13 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
     assert call(greedy=1, temperature=0.0, top_p=3.0) == 1       # still no workspace
     p = P(*[dict(good)[f] for f, _ in P._fields_])
     assert L.spec_verify(None, None, None, None, ctypes.byref(p), None, None) == 1
+
+
+def test_accept_histogram_rejects_bad_arguments_on_the_host(L):
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    assert L.spec_accept_histogram(fake, -1, 4, fake, None) == 1
+    assert L.spec_accept_histogram(fake, 3, 0, fake, None) == 1
+    assert L.spec_accept_histogram(fake, 3, 8193, fake, None) == 1
+    assert L.spec_accept_histogram(None, 3, 4, fake, None) == 1
+    assert L.spec_accept_histogram(fake, 3, 4, None, None) == 1
+    assert L.spec_accept_histogram(None, 0, 4, None, None) == 0   # nothing to count

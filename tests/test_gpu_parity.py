@@ -264,3 +264,45 @@ def test_worked_example_distribution_on_gpu(sv):
     ref = oracle.verify(np.stack([lt, lt])[None], ld[None, None], d, u, tgt_strides=(0, 4),
                         drf_strides=(0, 4), B=B)
     compare_verify(gt, gn, ref, "worked-example")
+
+
+def test_accept_histogram_matches_oracle(sv):
+    """Acceptance telemetry: the histogram the kernel adds to hist equals the
+    oracle's histogram of the oracle's accepted counts, bin for bin; a second call
+    accumulates; sequences that ended in an error land in bin K+1."""
+    alpha, K, B = 0.8, 4, 40_000
+    drf = np.array([0.4, 0.3, 0.2, 0.1, 0, 0, 0, 0])
+    tgt = alpha * drf + (1 - alpha) * np.array([0, 0, 0, 0, .25, .25, .25, .25])
+    with np.errstate(divide="ignore"):
+        lt, ld = np.log(tgt).astype(np.float32), np.log(drf).astype(np.float32)
+    rng = np.random.default_rng(31)
+    d = np.stack([rng.choice(8, size=B, p=drf) for _ in range(K)], 1).astype(np.int32)
+    u = rng.random((B, K + 1))
+    d[:7, 1] = 8                                     # out-of-range draft tokens: errors
+    target = np.ascontiguousarray(np.broadcast_to(lt, (B, K + 1, 8)))
+    draft = np.ascontiguousarray(np.broadcast_to(ld, (B, K, 8)))
+    out_t, out_n = sv.spec_verify(to_dev(target), to_dev(draft), to_dev(d), to_dev(u))
+    ref = oracle.verify(target, draft, d, u)
+    ok = ref["flags"] == 0
+    gn = out_n.cpu().numpy()
+    assert np.array_equal(gn[ok], ref["num_accepted"][ok])
+    hist = sv.spec_accept_histogram(out_n, K)
+    torch.cuda.synchronize()
+    want = oracle.accept_histogram(gn, K)
+    assert np.array_equal(hist.cpu().numpy(), want)
+    assert want[K + 1] == 7
+    assert np.array_equal(oracle.accept_histogram(ref["num_accepted"][ok], K), oracle.accept_histogram(gn[ok], K))
+    sv.spec_accept_histogram(out_n, K, hist=hist)
+    torch.cuda.synchronize()
+    assert np.array_equal(hist.cpu().numpy(), 2 * want)
+    # a full-size call's histogram (c5 shape) against the oracle's
+    w = workloads.make("c5", B=4)
+    prm = params_of(w)
+    dd = oracle.sample_draft(w["draft"], w["u_draft"], **prm)["tokens"]
+    o_t, o_n = sv.spec_verify(to_dev(w["target"]), to_dev(w["draft"]), to_dev(dd), to_dev(w["u_verify"]), **prm)
+    h5 = sv.spec_accept_histogram(o_n, w["K"])
+    torch.cuda.synchronize()
+    r5 = oracle.verify(w["target"], w["draft"], dd, w["u_verify"], **prm)
+    keep = r5["flags"] == 0
+    assert np.array_equal(o_n.cpu().numpy()[keep], r5["num_accepted"][keep])
+    assert np.array_equal(h5.cpu().numpy(), oracle.accept_histogram(o_n.cpu().numpy(), w["K"]))

@@ -108,6 +108,50 @@ def test_expected_tokens_per_round_closed_form(alpha, K):
     assert abs(n1.mean() - want) < 4 * n1.std() / math.sqrt(B)
 
 
+@pytest.mark.parametrize("alpha,K", [(0.8, 4), (0.5, 3)])
+def test_accept_histogram_follows_truncated_geometric_law(alpha, K):
+    """Acceptance telemetry ("Speculative decoding: how to run large models faster",
+    "Limitations and open issues").  With acceptance alpha at every position the
+    accept tests are independent, so a round accepts j < K tokens with probability
+    alpha^j (1 - alpha) and all K with alpha^K; the histogram's mean tokens per
+    round is then the printed closed form."""
+    drf = np.array([0.4, 0.3, 0.2, 0.1, 0, 0, 0, 0])
+    tgt = alpha * drf + (1 - alpha) * np.array([0, 0, 0, 0, .25, .25, .25, .25])
+    lt, ld = logits_of(tgt), logits_of(drf)
+    dp = probs_of(ld)
+    B = 100_000
+    rng = np.random.default_rng(9)
+    d = np.stack([rng.choice(8, size=B, p=dp) for _ in range(K)], 1).astype(np.int32)
+    u = rng.random((B, K + 1))
+    d[:50, 0] = 8                                   # 50 sequences with an out-of-range token
+    res = oracle.verify(_repeat_rows([lt] * (K + 1)), _repeat_rows([ld] * K), d, u,
+                        tgt_strides=(0, 8), drf_strides=(0, 8), B=B)
+    hist = oracle.accept_histogram(res["num_accepted"], K)
+    assert hist.shape == (K + 2,) and hist.sum() == B and hist[K + 1] == 50
+    ok = B - 50
+    law = np.array([alpha ** j * (1 - alpha) for j in range(K)] + [alpha ** K])
+    assert stats.chisquare(hist[:K + 1], law * ok).pvalue > 1e-4
+    mean_tokens = (np.arange(1, K + 2) * hist[:K + 1]).sum() / ok
+    want = (1 - alpha ** (K + 1)) / (1 - alpha)
+    assert abs(mean_tokens - want) < 4 * math.sqrt(K * K / ok)
+
+
+def test_accept_histogram_bins_every_value():
+    """Bins 0..K count exactly the sequences with that many accepted tokens; every
+    other value (an error) lands in bin K+1 -- checked on all values in [-3, K+3]."""
+    K = 5
+    vals = np.arange(-3, K + 4, dtype=np.int32)
+    counts = np.arange(1, vals.size + 1)
+    n = np.repeat(vals, counts)
+    np.random.default_rng(2).shuffle(n)
+    hist = oracle.accept_histogram(n, K)
+    for v, c in zip(vals, counts):
+        if 0 <= v <= K:
+            assert hist[v] == c
+    assert hist[K + 1] == counts[(vals < 0) | (vals > K)].sum()
+    assert hist.sum() == n.size
+
+
 # --------------------------------------------------------------------------
 # Theorem 1 and brute force
 

@@ -106,3 +106,72 @@ def make(cfg: Config | str, B: int | None = None, V: int | None = None, K: int |
     return dict(target=target, draft=draft, u_draft=u_draft, u_verify=u_verify,
                 temperature=cfg.temperature, top_k=cfg.top_k, top_p=cfg.top_p,
                 greedy=cfg.greedy, B=B, K=K, V=V, dtype=cfg.dtype, name=cfg.name)
+
+
+# --------------------------------------------------------------------------
+# Synthetic logit sources for the decode-round driver.
+#
+# The decode loop of the pages ("Speculative Decoding", roadtointelligence.com,
+# section "Draft, then verify"; Algorithm 2 in the paperlayer.ai summary of
+# "Accelerating Large Language Model Decoding with Speculative Sampling") calls
+# a draft and a target model.  No weights are available, so each "model" here
+# is a seeded table of S logit rows, and the row for a context is picked by a
+# state computed from the context's last token and its position:
+#     state = (last_token * STATE_A + position * STATE_B) mod S.
+# Both the GPU driver and the oracle's loop index the same tables with the same
+# integer formula, so they see bit-identical rows.
+
+STATE_A, STATE_B = 7919, 104729
+
+
+def state_of(last_token, position, S):
+    """State index of a context (numpy or torch integer arrays; int64 math)."""
+    return (last_token * STATE_A + position * STATE_B) % S
+
+
+@dataclasses.dataclass
+class SyntheticSource:
+    V: int
+    S: int
+    target: np.ndarray      # [S, V] float32 logits (or uint16 bf16 bits)
+    draft: np.ndarray       # [S, V]
+    alpha: float | None     # the exact acceptance of every state, when built for one
+    dtype: str
+
+
+def synthetic_source(V=256, S=97, alpha=None, seed=0, dtype="f32", sigma_draft=1.0):
+    """Target and draft tables of S rows.
+
+    alpha=None: Zipf+Gaussian target rows as in make() and draft = target +
+    N(0, sigma_draft^2).  alpha given: every state has sum_x min(p, q) = alpha
+    exactly (in the probabilities the logits are the logs of): the draft q lives on
+    tokens [0, V/2) with q = softmax(N(0, 1.5^2)) there; the target is
+    p = alpha * q + (1 - alpha) * r with r uniform on [V/2, V), where q = 0.
+    """
+    rng = np.random.default_rng(seed)
+    if alpha is None:
+        perm = rng.permutation(V)
+        bias = (np.float32(-1.1) * np.log((1 + perm).astype(np.float32))).astype(np.float32)
+        target = rng.standard_normal((S, V), dtype=np.float32) * np.float32(3.0) + bias
+        draft = target + rng.standard_normal((S, V), dtype=np.float32) * np.float32(sigma_draft)
+    else:
+        h = V // 2
+        g = rng.standard_normal((S, h)) * 1.5
+        q = np.exp(g - g.max(axis=1, keepdims=True))
+        q /= q.sum(axis=1, keepdims=True)
+        qf = np.zeros((S, V))
+        qf[:, :h] = q
+        r = np.zeros((S, V))
+        r[:, h:] = 1.0 / (V - h)
+        p = alpha * qf + (1 - alpha) * r
+        with np.errstate(divide="ignore"):
+            target, draft = np.log(p).astype(np.float32), np.log(qf).astype(np.float32)
+    if dtype == "bf16":
+        target, draft = to_bf16_bits(target), to_bf16_bits(draft)
+    return SyntheticSource(V, S, np.ascontiguousarray(target), np.ascontiguousarray(draft), alpha, dtype)
+
+
+def round_uniforms(seed, r, B, K):
+    """Uniforms of decode round r: u_draft [B, K] (draft draws), u_verify [B, K+1]."""
+    rng = np.random.default_rng([int(seed), int(r)])
+    return rng.random((B, K)), rng.random((B, K + 1))
