@@ -503,6 +503,36 @@ def run_sweep_k(args):
         torch.cuda.synchronize(dev)
         us = e0.elapsed_time(e1) * 1e3 / n
         rows.append({"K": K, "verify_us": us, "rows": w["B"] * (2 * K + 1)})
+    # K = 1: the fused drafting step + verification against the two separate calls
+    w = workloads.make("c5", K=1)
+    prm = dict(temperature=w["temperature"], top_k=w["top_k"], top_p=w["top_p"], greedy=w["greedy"])
+    conv = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    tgt, drf = conv(w["target"]), conv(w["draft"])
+    ud2 = torch.from_numpy(w["u_draft"]).to(dev)
+    ud1 = ud2[:, 0].contiguous()
+    uv = torch.from_numpy(w["u_verify"]).to(dev)
+
+    def fused():
+        sv.spec_sample_verify(tgt, drf, ud1, uv, **prm)
+
+    def separate():
+        d = sv.spec_sample_draft(drf, ud2, **prm)
+        sv.spec_verify(tgt, drf, d, uv, **prm)
+
+    k1 = {}
+    for nm, fn in (("fused_us", fused), ("separate_us", separate)):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(50):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        k1[nm] = e0.elapsed_time(e1) * 1e3 / 50
+    k1["bytes_fused"] = w["B"] * 3 * w["V"] * 2
+    k1["bytes_separate"] = w["B"] * 4 * w["V"] * 2
     vc = {r["K"]: r["verify_us"] / 1e3 / t_target for r in rows}
     model = []
     for alpha in (0.75, 0.8):
@@ -513,7 +543,8 @@ def run_sweep_k(args):
                       "best_k_without_verify": decode.best_k(alpha, c, lambda k: 0.0, 8)})
     line = {"mode": "sweep_k", "metric": "spec_verify time vs K (c5 shape) and modelled speed-up",
             "workload": "c5 with K = 1..8 (B=32, V=256000 bf16, top_k=50)", "verify": rows,
-            "model": model, "t_target_ms": t_target, "t_draft_ms": t_draft}
+            "model": model, "t_target_ms": t_target, "t_draft_ms": t_draft,
+            "k1_sample_verify": k1}
     print(json.dumps(line), flush=True)
     return 0
 

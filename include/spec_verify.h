@@ -141,6 +141,27 @@ spec_status spec_verify(const void* target_logits, const void* draft_logits,
                         const spec_params* params, int32_t* out_tokens,
                         int32_t* out_num_accepted);
 
+/* Drafting step and verification fused, for K = 1: draw each sequence's one
+ * draft token from its draft row (as spec_sample_draft), then verify it against
+ * the two target rows (as spec_verify with that token) -- in one call, so the
+ * draft row is read once.  The result is the same as the two calls in a row
+ * with the same uniforms.  ("Speculative Decoding", section "Draft, then
+ * verify", steps 1-4, with a lookahead of one token.)
+ *   target_logits     device [B, 2, V] rows (target strides)
+ *   draft_logits      device [B, 1, V] rows (draft strides)
+ *   draft_uniforms    device fp64 [B]: the draft draws
+ *   uniforms          device fp64 [B, 2]: column 0 the accept test, column 1
+ *                     the final draw
+ *   out_draft_tokens  device int32 [B]: the drawn draft tokens (-1 for a row
+ *                     with an error)
+ *   out_tokens, out_num_accepted  as spec_verify with K = 1
+ * params->K must be 1 and params->greedy 0 (else SPEC_ERR_INVALID_ARG); the
+ * workspace is spec_verify_workspace_size(params). */
+spec_status spec_sample_verify(const void* target_logits, const void* draft_logits,
+                               const double* draft_uniforms, const double* uniforms,
+                               const spec_params* params, int32_t* out_draft_tokens,
+                               int32_t* out_tokens, int32_t* out_num_accepted);
+
 /* Draw the K draft tokens of each sequence from the adjusted draft distribution
  * (same temperature / top-k / top-p / greedy as verification), one inverse-CDF
  * draw per row in index order ("Speculative Decoding", section "Draft, then

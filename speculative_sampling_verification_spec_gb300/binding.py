@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_CUDA", 3: 
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
 EXPORTED = ("spec_verify", "spec_sample_draft", "spec_verify_workspace_size",
             "spec_sample_draft_workspace_size", "spec_read_row_stats", "spec_status_string",
-            "spec_launch_count", "spec_verify_noalloc", "spec_accept_histogram")
+            "spec_launch_count", "spec_verify_noalloc", "spec_accept_histogram", "spec_sample_verify")
 
 
 class SpecParams(ctypes.Structure):
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.spec_status_string.restype = ctypes.c_char_p
             L.spec_verify_noalloc.argtypes = [P, P, P, P, PP, P, P]
             L.spec_verify_noalloc.restype = ctypes.c_int
+            L.spec_sample_verify.argtypes = [P, P, P, P, PP, P, P, P]
+            L.spec_sample_verify.restype = ctypes.c_int
             L.spec_accept_histogram.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
             L.spec_accept_histogram.restype = ctypes.c_int
             L.spec_launch_count.argtypes = []
@@ -275,3 +277,43 @@ def spec_accept_histogram(out_num_accepted, K, *, hist=None, stream=None):
     if code != SPEC_OK:
         raise SpecError(code, "spec_accept_histogram")
     return hist
+
+
+def spec_sample_verify(target, draft, draft_uniforms, uniforms, *, temperature=1.0, top_k=0, top_p=1.0,
+                       greedy=False, out_draft_tokens=None, out_tokens=None, out_num_accepted=None, status=None,
+                       ws=None, stream=None):
+    """K = 1 drafting step and verification in one call: target [B, 2, V] and draft
+    [B, 1, V] CUDA logits, draft_uniforms [B] and uniforms [B, 2] float64.
+    Returns (out_draft_tokens [B], out_tokens [B, 2], out_num_accepted [B]), int32.
+    Sampling only (greedy has no draft draw to fuse)."""
+    if greedy:
+        raise ValueError("spec_sample_verify samples; use spec_sample_draft + spec_verify for greedy")
+    _check_cuda(target, draft, draft_uniforms, uniforms)
+    B, V = target.shape[0], target.shape[-1]
+    if target.shape[1] != 2 or draft.shape[1] != 1:
+        raise ValueError("spec_sample_verify takes K = 1: target [B, 2, V], draft [B, 1, V]")
+    if draft.dtype != target.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    if target.stride(-1) != 1 or draft.stride(-1) != 1:
+        raise ValueError("logit rows must be contiguous along the vocabulary")
+    if draft_uniforms.dtype != torch.float64 or uniforms.dtype != torch.float64:
+        raise TypeError("uniforms must be float64")
+    dev = target.device
+    if out_draft_tokens is None:
+        out_draft_tokens = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, 2), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    p = make_params(B, 1, V, _dtype_code(target), (target.stride(0), target.stride(1)),
+                    (draft.stride(0), draft.stride(1)), temperature, top_k, top_p, False,
+                    _stream_handle(stream), status)
+    if ws is None:
+        ws = workspace(int(lib().spec_verify_workspace_size(ctypes.byref(p))), dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    code = lib().spec_sample_verify(_ptr(target), _ptr(draft), _ptr(draft_uniforms.contiguous()),
+                                    _ptr(uniforms.contiguous()), ctypes.byref(p), _ptr(out_draft_tokens),
+                                    _ptr(out_tokens), _ptr(out_num_accepted))
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_sample_verify")
+    return out_draft_tokens, out_tokens, out_num_accepted

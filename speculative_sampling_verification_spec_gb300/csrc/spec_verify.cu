@@ -324,6 +324,9 @@ struct KArgs {
   uint32_t rows_m, rows_s;  // the same for rows per sequence (verify: R, sample: K)
   int seg_bytes;        // bytes of one segment buffer in shared memory
   int mode, greedy, top_k, aligned;
+  int fused;            // verify with K = 1 whose draft token is drawn in the same call
+  const double* u_draft;  // fused: [B] uniforms of the draft draws
+  int32_t* out_draft;     // fused: [B] the drawn draft tokens (tokens aliases it)
   int need_z;           // segments sum the normaliser (no filter, or top-p without top-k)
   int filt, n0;         // segments list candidates; theta is the n0-th thread maximum
   float top_p, c, temp;
@@ -1307,10 +1310,25 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
   for (int r = tid; r < R; r += kThreads) myfl |= __ldcg(&recs[r].flags);
   {
     for (int t = tid; t < K; t += kThreads) {
-      const int d = a.tokens[static_cast<int64_t>(b) * K + t];
+      const int d = a.fused ? __ldcg(&a.out_draft[b]) : a.tokens[static_cast<int64_t>(b) * K + t];
       bool acc;
       if (a.greedy) {
         acc = (d == __ldcg(&recs[t].argmax));
+      } else if (a.fused) {
+        // the token was drawn by the draft row of this call: its probabilities
+        // under both adjusted rows, with the arithmetic of the row records
+        const E* gt = static_cast<const E*>(a.tgt) + static_cast<int64_t>(b) * a.tgt_seq;
+        const E* gd = static_cast<const E*>(a.drf) + static_cast<int64_t>(b) * a.drf_seq;
+        auto prob = [&](const E* g, const spec_row_stat& r) -> double {
+          if (d < 0 || d >= a.V) return 0.0;
+          const float l = Fmt<E>::at_global(g, d);
+          const Cut c{__ldcg(&r.tau_val), __ldcg(&r.tau_idx)};
+          if (!(c.keep(l, d) && l > -INFINITY)) return 0.0;
+          return static_cast<double>(wexp(l, __ldcg(&r.m), a.c)) / __ldcg(&r.zf);
+        };
+        const double pt = prob(gt, recs[t]);
+        const double pd = prob(gd, recs[K + 1 + t]);
+        acc = a.u[static_cast<int64_t>(b) * (K + 1) + t] * pd < pt;
       } else {
         // keep d_t with probability min(1, tgt/drf):  u * drf < tgt
         const double pt = __ldcg(&recs[t].p_tok);
@@ -1333,7 +1351,8 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
     }
     return;
   }
-  for (int t = tid; t <= K; t += kThreads) out[t] = (t < n) ? a.tokens[static_cast<int64_t>(b) * K + t] : -1;
+  for (int t = tid; t <= K; t += kThreads)
+    out[t] = (t < n) ? (a.fused ? __ldcg(&a.out_draft[b]) : a.tokens[static_cast<int64_t>(b) * K + t]) : -1;
   int token;
   if (a.greedy) {
     token = __ldcg(&recs[n].argmax);
@@ -1771,9 +1790,10 @@ __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scr
     if (!done) general_cut<E>(a, rg, sm, C, sb, z, &cut, &zf, &list_len, lidx, lw);
   }
 
-  // sample mode: draw this row's token
-  if (a.mode == kModeSample) {
-    const double u = a.greedy ? 0.0 : a.u[static_cast<int64_t>(ri.b) * a.K + ri.t];
+  // sample mode (and the draft row of a fused call): draw this row's token
+  const bool draws = a.mode == kModeSample || (a.fused && !ri.is_target);
+  if (draws) {
+    const double u = a.greedy ? 0.0 : a.fused ? a.u_draft[ri.b] : a.u[static_cast<int64_t>(ri.b) * a.K + ri.t];
     int tok;
     if (bad) {
       tok = -1;
@@ -1787,7 +1807,8 @@ __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scr
       tok = global_rows_draw<E>(a, grow, grow, m, m, cut, cut, 1.0f, 1.0f, false, u, sm);
     }
     if (tid == 0) {
-      a.out_tokens[static_cast<int64_t>(ri.b) * a.K + ri.t] = tok;
+      if (a.fused) a.out_draft[ri.b] = tok;
+      else a.out_tokens[static_cast<int64_t>(ri.b) * a.K + ri.t] = tok;
       rec->token = tok;
     }
   }
@@ -1797,7 +1818,7 @@ __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scr
     int flags = 0;
     if (bad) flags |= kFlagNonfinite;
     double p_tok = 0.0;
-    if (a.mode == kModeVerify && ri.t < a.K) {
+    if (a.mode == kModeVerify && ri.t < a.K && !a.fused) {  // fused: the epilogue computes it
       const int d = a.tokens[static_cast<int64_t>(ri.b) * a.K + ri.t];
       if (d < 0 || d >= a.V) {
         flags |= kFlagToken;
@@ -2623,6 +2644,49 @@ spec_status spec_verify(const void* target_logits, const void* draft_logits, con
   a.out_n = out_num_accepted;
   a.mode = kModeVerify;
   a.aligned = al ? 1 : 0;
+  fill_common(p, pl, a);
+  fill_rows_div(a);
+  return launch(p, pl, a, di);
+}
+
+spec_status spec_sample_verify(const void* target_logits, const void* draft_logits, const double* draft_uniforms,
+                               const double* uniforms, const spec_params* params, int32_t* out_draft_tokens,
+                               int32_t* out_tokens, int32_t* out_num_accepted) {
+  if (!params) return SPEC_ERR_INVALID_ARG;
+  if (params->K != 1 || params->greedy) return SPEC_ERR_INVALID_ARG;
+  Plan pl;
+  spec_status s = make_plan(params, true, &pl);
+  if (s != SPEC_OK) return s;
+  const spec_params* p = params;
+  if (p->B == 0) return SPEC_OK;
+  if (!target_logits || !draft_logits || !draft_uniforms || !uniforms || !out_draft_tokens || !out_tokens ||
+      !out_num_accepted)
+    return SPEC_ERR_INVALID_ARG;
+  if (!workspace_ok(p, pl)) return SPEC_ERR_INVALID_ARG;
+  DevInfo* di = nullptr;
+  if (!dev_info(&di)) return SPEC_ERR_CUDA;
+  s = plan_launch(p, *di, &pl);
+  if (s != SPEC_OK) return s;
+  const int64_t es = pl.esize;
+  const bool al = aligned16(target_logits) && (p->target_seq_stride * es) % 16 == 0 &&
+                  (p->target_row_stride * es) % 16 == 0 && aligned16(draft_logits) &&
+                  (p->draft_seq_stride * es) % 16 == 0 && (p->draft_row_stride * es) % 16 == 0;
+  KArgs a = {};
+  a.tgt = target_logits;
+  a.drf = draft_logits;
+  a.tgt_seq = p->target_seq_stride;
+  a.tgt_row = p->target_row_stride;
+  a.drf_seq = p->draft_seq_stride;
+  a.drf_row = p->draft_row_stride;
+  a.tokens = out_draft_tokens;  // written by the draft rows, read by the sequence epilogue
+  a.u = uniforms;
+  a.out_tokens = out_tokens;
+  a.out_n = out_num_accepted;
+  a.mode = kModeVerify;
+  a.aligned = al ? 1 : 0;
+  a.fused = 1;
+  a.u_draft = draft_uniforms;
+  a.out_draft = out_draft_tokens;
   fill_common(p, pl, a);
   fill_rows_div(a);
   return launch(p, pl, a, di);

@@ -102,3 +102,29 @@ def test_accept_histogram_rejects_bad_arguments_on_the_host(L):
     assert L.spec_accept_histogram(None, 3, 4, fake, None) == 1
     assert L.spec_accept_histogram(fake, 3, 4, None, None) == 1
     assert L.spec_accept_histogram(None, 0, 4, None, None) == 0   # nothing to count
+
+
+def test_sample_verify_requires_k1_sampling_on_the_host(L):
+    from speculative_sampling_verification_spec_gb300 import binding as b
+    P = b.SpecParams
+    good = dict(B=2, K=1, V=16, dtype=b.SPEC_F32, target_seq_stride=32, target_row_stride=16,
+                draft_seq_stride=16, draft_row_stride=16, temperature=1.0, top_k=0, top_p=1.0,
+                greedy=0, stream=None, status=None, workspace=None, workspace_bytes=0)
+
+    def call(ptrs=None, **over):
+        kw = dict(good, **over)
+        p = P(*[kw[f] for f, _ in P._fields_])
+        fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+        args = ptrs if ptrs is not None else [fake] * 7
+        return L.spec_sample_verify(args[0], args[1], args[2], args[3], ctypes.byref(p), args[4], args[5],
+                                    args[6])
+
+    assert call(K=2) == 1                    # K = 1 only
+    assert call(greedy=1) == 1               # sampling only
+    assert call(temperature=0.0) == 1
+    assert call() == 1                       # no workspace
+    fake = ctypes.c_void_p(0x1000)
+    assert call(ptrs=[fake, fake, None, fake, fake, fake, fake]) == 1   # draft uniforms missing
+    assert call(ptrs=[fake, fake, fake, fake, None, fake, fake]) == 1   # draft-token output missing
+    assert call(B=0) == 0
+    assert L.spec_sample_verify(None, None, None, None, None, None, None, None) == 1

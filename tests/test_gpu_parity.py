@@ -306,3 +306,36 @@ def test_accept_histogram_matches_oracle(sv):
     keep = r5["flags"] == 0
     assert np.array_equal(o_n.cpu().numpy()[keep], r5["num_accepted"][keep])
     assert np.array_equal(h5.cpu().numpy(), oracle.accept_histogram(o_n.cpu().numpy(), w["K"]))
+
+
+@pytest.mark.parametrize("name,kw,prm", [
+    ("c2", dict(K=1, B=64), {}),
+    ("c3", dict(K=1, B=32), {}),
+    ("c5", dict(K=1, B=16), {}),
+    ("c5", dict(K=1, B=24, V=70003), {}),
+    ("c1", dict(K=1, B=256), dict(top_k=5, top_p=0.9, temperature=1.3))])
+def test_sample_verify_equals_draw_then_verify(sv, name, kw, prm):
+    """The fused K = 1 step gives the oracle's draw from the draft row, then the
+    oracle's verification of that token: draft token, emitted tokens and count."""
+    w = workloads.make(name, **kw)
+    p = dict(params_of(w), **prm)
+    assert w["K"] == 1 and not p["greedy"]
+    ud = w["u_draft"][:, 0].copy()
+    dr = oracle.sample_draft(w["draft"], w["u_draft"], **p)
+    ref = oracle.verify(w["target"], w["draft"], dr["tokens"], w["u_verify"], **p)
+    assert ref["status"] == oracle.OK
+    g_d, g_t, g_n = sv.spec_sample_verify(to_dev(w["target"]), to_dev(w["draft"]), to_dev(ud),
+                                          to_dev(w["u_verify"]), **p)
+    torch.cuda.synchronize()
+    g_d, g_t, g_n = g_d.cpu().numpy(), g_t.cpu().numpy(), g_n.cpu().numpy()
+    ok = (dr["flags"][:, 0] == 0) & (ref["flags"] == 0)
+    assert ok.sum() >= 0.9 * w["B"]
+    assert np.array_equal(g_d[ok], dr["tokens"][ok, 0])
+    assert np.array_equal(g_n[ok], ref["num_accepted"][ok])
+    assert np.array_equal(g_t[ok], ref["tokens"][ok])
+    # and the same as the two separate calls on the GPU
+    s_d = sv.spec_sample_draft(to_dev(w["draft"]), to_dev(w["u_draft"]), **p)
+    s_t, s_n = sv.spec_verify(to_dev(w["target"]), to_dev(w["draft"]), s_d, to_dev(w["u_verify"]), **p)
+    torch.cuda.synchronize()
+    assert np.array_equal(s_d.cpu().numpy()[:, 0], g_d)
+    assert np.array_equal(s_n.cpu().numpy(), g_n) and np.array_equal(s_t.cpu().numpy(), g_t)
