@@ -533,6 +533,28 @@ def run_sweep_k(args):
         k1[nm] = e0.elapsed_time(e1) * 1e3 / 50
     k1["bytes_fused"] = w["B"] * 3 * w["V"] * 2
     k1["bytes_separate"] = w["B"] * 4 * w["V"] * 2
+    # ragged batch at the c5 shape: draft lengths spread over 1..8, against the padded call
+    w = workloads.make("c5")
+    prm = dict(temperature=w["temperature"], top_k=w["top_k"], top_p=w["top_p"], greedy=w["greedy"])
+    tgt, drf = conv(w["target"]), conv(w["draft"])
+    tok = sv.spec_sample_draft(drf, torch.from_numpy(w["u_draft"]).to(dev), **prm)
+    uv = torch.from_numpy(w["u_verify"]).to(dev)
+    lens = (np.arange(w["B"]) % w["K"] + 1).astype(np.int32)
+    rg = {}
+    for nm, fn in (("ragged_us", lambda: sv.spec_verify_ragged(tgt, drf, tok, uv, lens, **prm)),
+                   ("padded_us", lambda: sv.spec_verify(tgt, drf, tok, uv, **prm))):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(50):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        rg[nm] = e0.elapsed_time(e1) * 1e3 / 50
+    rg["rows_ragged"] = int((2 * lens + 1).sum())
+    rg["rows_padded"] = w["B"] * (2 * w["K"] + 1)
     vc = {r["K"]: r["verify_us"] / 1e3 / t_target for r in rows}
     model = []
     for alpha in (0.75, 0.8):
@@ -544,7 +566,7 @@ def run_sweep_k(args):
     line = {"mode": "sweep_k", "metric": "spec_verify time vs K (c5 shape) and modelled speed-up",
             "workload": "c5 with K = 1..8 (B=32, V=256000 bf16, top_k=50)", "verify": rows,
             "model": model, "t_target_ms": t_target, "t_draft_ms": t_draft,
-            "k1_sample_verify": k1}
+            "k1_sample_verify": k1, "ragged_c5": rg}
     print(json.dumps(line), flush=True)
     return 0
 

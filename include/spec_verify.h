@@ -141,6 +141,34 @@ spec_status spec_verify(const void* target_logits, const void* draft_logits,
                         const spec_params* params, int32_t* out_tokens,
                         int32_t* out_num_accepted);
 
+/* Workspace bytes spec_verify_ragged needs (0 if the parameters are invalid):
+ * the bytes of spec_verify with K the longest draft, plus the rows' index. */
+size_t spec_verify_ragged_workspace_size(const spec_params* params);
+
+/* Verification of a ragged batch: sequence b has its own draft length
+ * 1 <= draft_lengths[b] <= K, and only its K_b + 1 target rows and K_b draft
+ * rows are read ("Speculative Decoding", section "Draft, then verify", per
+ * sequence; in a serving batch the sequences' lookaheads differ).  The result
+ * for each sequence is spec_verify's with K = K_b.
+ *   target_logits, draft_logits  device [B, K+1, V] / [B, K, V] rows (strides as
+ *                     spec_verify); rows past a sequence's length are not read
+ *   draft_tokens      device int32 [B, K]; columns >= K_b are not read
+ *   uniforms          device fp64 [B, K+1]: column t < K_b the accept test at t,
+ *                     column K_b the final draw (later columns are not read);
+ *                     may be NULL when greedy
+ *   draft_lengths     HOST int32 [B]: K_b (read before the call returns)
+ *   params            as spec_verify, with K = the longest draft; the workspace
+ *                     is spec_verify_ragged_workspace_size(params) bytes
+ *   out_tokens        device int32 [B, K+1]: the n accepted tokens, the emitted
+ *                     token, then -1 up to column K
+ *   out_num_accepted  device int32 [B]: n in [0, K_b], or -1 on an error
+ * Returns SPEC_ERR_INVALID_ARG (nothing launched) for a length outside [1, K]
+ * or a NULL draft_lengths, plus spec_verify's checks. */
+spec_status spec_verify_ragged(const void* target_logits, const void* draft_logits,
+                               const int32_t* draft_tokens, const double* uniforms,
+                               const int32_t* draft_lengths, const spec_params* params,
+                               int32_t* out_tokens, int32_t* out_num_accepted);
+
 /* Drafting step and verification fused, for K = 1: draw each sequence's one
  * draft token from its draft row (as spec_sample_draft), then verify it against
  * the two target rows (as spec_verify with that token) -- in one call, so the

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_CUDA", 3: 
 SPEC_NOALLOC_SCRATCH_BYTES = 8 << 20
 EXPORTED = ("spec_verify", "spec_sample_draft", "spec_verify_workspace_size",
             "spec_sample_draft_workspace_size", "spec_read_row_stats", "spec_status_string",
-            "spec_launch_count", "spec_verify_noalloc", "spec_accept_histogram", "spec_sample_verify")
+            "spec_launch_count", "spec_verify_noalloc", "spec_accept_histogram", "spec_sample_verify",
+            "spec_verify_ragged", "spec_verify_ragged_workspace_size")
 
 
 class SpecParams(ctypes.Structure):
@@ -85,6 +86,10 @@ def lib() -> ctypes.CDLL:
             L.spec_status_string.restype = ctypes.c_char_p
             L.spec_verify_noalloc.argtypes = [P, P, P, P, PP, P, P]
             L.spec_verify_noalloc.restype = ctypes.c_int
+            L.spec_verify_ragged.argtypes = [P, P, P, P, P, PP, P, P]
+            L.spec_verify_ragged.restype = ctypes.c_int
+            L.spec_verify_ragged_workspace_size.argtypes = [PP]
+            L.spec_verify_ragged_workspace_size.restype = ctypes.c_size_t
             L.spec_sample_verify.argtypes = [P, P, P, P, PP, P, P, P]
             L.spec_sample_verify.restype = ctypes.c_int
             L.spec_accept_histogram.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
@@ -317,3 +322,46 @@ def spec_sample_verify(target, draft, draft_uniforms, uniforms, *, temperature=1
     if code != SPEC_OK:
         raise SpecError(code, "spec_sample_verify")
     return out_draft_tokens, out_tokens, out_num_accepted
+
+
+def spec_verify_ragged(target, draft, draft_tokens, uniforms, draft_lengths, *, temperature=1.0, top_k=0,
+                       top_p=1.0, greedy=False, out_tokens=None, out_num_accepted=None, status=None, ws=None,
+                       stream=None):
+    """spec_verify with a draft length per sequence: target [B, K+1, V], draft
+    [B, K, V] CUDA logits, draft_tokens [B, K], uniforms [B, K+1] (column K_b: the
+    final draw), draft_lengths: host ints K_b in [1, K] (list, numpy or CPU tensor).
+    Returns (out_tokens [B, K+1], out_num_accepted [B])."""
+    import numpy as np
+    _check_cuda(target, draft, draft_tokens, uniforms)
+    K = draft_tokens.shape[1]
+    B, V = draft_tokens.shape[0], target.shape[-1]
+    lens = np.ascontiguousarray(np.asarray(draft_lengths.cpu() if torch.is_tensor(draft_lengths) else draft_lengths,
+                                           dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("draft_lengths must hold one length per sequence")
+    dt = _dtype_code(target)
+    if draft is not None and draft.dtype != target.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    if target.stride(-1) != 1 or (draft is not None and draft.stride(-1) != 1):
+        raise ValueError("logit rows must be contiguous along the vocabulary")
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    dstr = (draft.stride(0), draft.stride(1)) if draft is not None else (0, 0)
+    p = make_params(B, K, V, dt, (target.stride(0), target.stride(1)), dstr, temperature, top_k, top_p, greedy,
+                    _stream_handle(stream), status)
+    if ws is None:
+        ws = workspace(int(lib().spec_verify_ragged_workspace_size(ctypes.byref(p))), dev)
+    p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    tok = draft_tokens if draft_tokens.dtype == torch.int32 else draft_tokens.to(torch.int32)
+    if uniforms is not None and uniforms.dtype != torch.float64:
+        raise TypeError("uniforms must be float64")
+    code = lib().spec_verify_ragged(_ptr(target), _ptr(draft), _ptr(tok.contiguous()),
+                                    _ptr(None if uniforms is None else uniforms.contiguous()),
+                                    lens.ctypes.data_as(ctypes.c_void_p), ctypes.byref(p), _ptr(out_tokens),
+                                    _ptr(out_num_accepted))
+    if code != SPEC_OK:
+        raise SpecError(code, "spec_verify_ragged")
+    return out_tokens, out_num_accepted

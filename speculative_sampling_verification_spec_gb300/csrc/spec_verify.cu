@@ -43,6 +43,7 @@
 #include <cstring>
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "spec_verify.h"
 
@@ -327,6 +328,7 @@ struct KArgs {
   int fused;            // verify with K = 1 whose draft token is drawn in the same call
   const double* u_draft;  // fused: [B] uniforms of the draft draws
   int32_t* out_draft;     // fused: [B] the drawn draft tokens (tokens aliases it)
+  const int32_t* row_start;  // ragged verify: [B + 1] first row of each sequence (NULL: R rows each)
   int need_z;           // segments sum the normaliser (no filter, or top-p without top-k)
   int filt, n0;         // segments list candidates; theta is the n0-th thread maximum
   float top_p, c, temp;
@@ -677,6 +679,7 @@ __device__ __forceinline__ unsigned long long sort_key(float v, int idx);
 
 struct RowInfo {
   int b, t, is_target, job;
+  int kb, first, nr;  // verify: the sequence's draft length, first row and row count
   int64_t row_off;  // element offset of the row from its tensor base
   int tok;          // draft token at this row (verify, t < K), else -1
 };
@@ -1187,20 +1190,59 @@ __device__ void kept_pass(const RowCtx<E>& rc, Scratch& sm, Local& C, Cut cut, b
 
 // ---------------------------------------------------------------------------
 
+// n / d for 0 <= n < 2^31 with the host's multiplier and shift for d
+__device__ __forceinline__ int fast_div(int n, uint32_t m, uint32_t s) {
+  return static_cast<int>((__umulhi(static_cast<uint32_t>(n), m) + static_cast<uint32_t>(n)) >> s);
+}
+
+// Ragged verification: the sequence of a row, by binary search in the prefix
+// of rows per sequence (row_start[b] <= row < row_start[b + 1]); its rows are
+// its K_b + 1 target rows, then (sampling) its K_b draft rows.
+struct SeqRows {
+  int b, first, nr, kb;
+};
+__device__ __forceinline__ SeqRows seq_of_row(const KArgs& a, int row) {
+  SeqRows q;
+  if (a.row_start) {
+    int lo = 0, hi = a.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(&a.row_start[mid]) <= row) lo = mid; else hi = mid;
+    }
+    q.b = lo;
+    q.first = __ldg(&a.row_start[lo]);
+    q.nr = __ldg(&a.row_start[lo + 1]) - q.first;
+    q.kb = a.greedy ? q.nr - 1 : (q.nr - 1) >> 1;
+  } else {
+    q.b = fast_div(row, a.rows_m, a.rows_s);
+    q.first = q.b * a.R;
+    q.nr = a.R;
+    q.kb = a.K;
+  }
+  return q;
+}
+
 __device__ RowInfo decode_job(const KArgs& a, int job) {
   RowInfo ri;
   ri.job = job;
   ri.tok = -1;
   if (a.mode == kModeVerify) {
-    ri.b = job / a.R;
-    const int r = job % a.R;
-    ri.is_target = r <= a.K;
-    ri.t = ri.is_target ? r : r - (a.K + 1);
+    const SeqRows q = seq_of_row(a, job);
+    ri.b = q.b;
+    ri.kb = q.kb;
+    ri.first = q.first;
+    ri.nr = q.nr;
+    const int r = job - q.first;
+    ri.is_target = r <= q.kb;
+    ri.t = ri.is_target ? r : r - (q.kb + 1);
     ri.row_off = ri.is_target ? static_cast<int64_t>(ri.b) * a.tgt_seq + static_cast<int64_t>(ri.t) * a.tgt_row
                               : static_cast<int64_t>(ri.b) * a.drf_seq + static_cast<int64_t>(ri.t) * a.drf_row;
   } else {
     ri.b = job / a.K;
     ri.t = job % a.K;
+    ri.kb = a.K;
+    ri.first = ri.b * a.K;
+    ri.nr = a.K;
     ri.is_target = 0;
     ri.row_off = static_cast<int64_t>(ri.b) * a.drf_seq + static_cast<int64_t>(ri.t) * a.drf_row;
   }
@@ -1297,10 +1339,14 @@ __device__ int global_rows_draw(const KArgs& a, const E* gt, const E* gd, float 
 // verify epilogue: the rank-0 CTA of the last cluster of sequence b
 
 template <typename E>
-__device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
-  const int K = a.K, R = a.R;
-  const spec_row_stat* recs = a.rows + static_cast<int64_t>(b) * R;
-  int32_t* out = a.out_tokens + static_cast<int64_t>(b) * (K + 1);
+// K = this sequence's draft length (ragged: K_b <= a.K); token, uniform and
+// output arrays keep the call's strides (a.K, a.K + 1), and the final draw
+// takes uniform column K.
+__device__ void verify_epilogue(const KArgs& a, int b, int K, int first, Scratch& sm) {
+  const int KS = a.K;  // strides of the [B, K] and [B, K + 1] arrays
+  const spec_row_stat* recs = a.rows + first;
+  const int R = a.greedy ? K + 1 : 2 * K + 1;
+  int32_t* out = a.out_tokens + static_cast<int64_t>(b) * (KS + 1);
   const int tid = threadIdx.x;
   // all row records in parallel, in one round of loads: the flags, and the
   // accept tests (one per thread; the flags decide afterwards whether they count)
@@ -1310,7 +1356,7 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
   for (int r = tid; r < R; r += kThreads) myfl |= __ldcg(&recs[r].flags);
   {
     for (int t = tid; t < K; t += kThreads) {
-      const int d = a.fused ? __ldcg(&a.out_draft[b]) : a.tokens[static_cast<int64_t>(b) * K + t];
+      const int d = a.fused ? __ldcg(&a.out_draft[b]) : a.tokens[static_cast<int64_t>(b) * KS + t];
       bool acc;
       if (a.greedy) {
         acc = (d == __ldcg(&recs[t].argmax));
@@ -1328,12 +1374,12 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
         };
         const double pt = prob(gt, recs[t]);
         const double pd = prob(gd, recs[K + 1 + t]);
-        acc = a.u[static_cast<int64_t>(b) * (K + 1) + t] * pd < pt;
+        acc = a.u[static_cast<int64_t>(b) * (KS + 1) + t] * pd < pt;
       } else {
         // keep d_t with probability min(1, tgt/drf):  u * drf < tgt
         const double pt = __ldcg(&recs[t].p_tok);
         const double pd = __ldcg(&recs[K + 1 + t].p_tok);
-        acc = a.u[static_cast<int64_t>(b) * (K + 1) + t] * pd < pt;
+        acc = a.u[static_cast<int64_t>(b) * (KS + 1) + t] * pd < pt;
       }
       if (!acc) atomicMin(&sm.bi[13], t);  // the first rejection wins
     }
@@ -1343,7 +1389,7 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
   const int fl = sm.bi[12], n = sm.bi[13];
   __syncthreads();
   if (fl) {
-    for (int t = tid; t <= K; t += kThreads) out[t] = -1;
+    for (int t = tid; t <= KS; t += kThreads) out[t] = -1;
     if (tid == 0) {
       a.out_n[b] = -1;
       set_status(a, (fl & kFlagToken) ? SPEC_ERR_TOKEN_RANGE
@@ -1351,20 +1397,20 @@ __device__ void verify_epilogue(const KArgs& a, int b, Scratch& sm) {
     }
     return;
   }
-  for (int t = tid; t <= K; t += kThreads)
-    out[t] = (t < n) ? (a.fused ? __ldcg(&a.out_draft[b]) : a.tokens[static_cast<int64_t>(b) * K + t]) : -1;
+  for (int t = tid; t <= KS; t += kThreads)
+    out[t] = (t < n) ? (a.fused ? __ldcg(&a.out_draft[b]) : a.tokens[static_cast<int64_t>(b) * KS + t]) : -1;
   int token;
   if (a.greedy) {
     token = __ldcg(&recs[n].argmax);
   } else {
-    const double u = a.u[static_cast<int64_t>(b) * (K + 1) + K];
+    const double u = a.u[static_cast<int64_t>(b) * (KS + 1) + K];
     const int rt = n, rd = K + 1 + n;
     const bool resid = n < K;
     const double zt = __ldcg(&recs[rt].zf);
     const double zd = resid ? __ldcg(&recs[rd].zf) : 1.0;
     const int lt = __ldcg(&recs[rt].list_len);
     const int ld = resid ? __ldcg(&recs[rd].list_len) : 0;
-    const int64_t job_t = static_cast<int64_t>(b) * R + rt, job_d = static_cast<int64_t>(b) * R + rd;
+    const int64_t job_t = static_cast<int64_t>(first) + rt, job_d = static_cast<int64_t>(first) + rd;
     if (lt >= 0 && ld >= 0) {
       // kept sets stored: residual over the target's kept list (index order)
       const int32_t* ti = a.list_idx + job_t * kCap;
@@ -1818,7 +1864,7 @@ __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scr
     int flags = 0;
     if (bad) flags |= kFlagNonfinite;
     double p_tok = 0.0;
-    if (a.mode == kModeVerify && ri.t < a.K && !a.fused) {  // fused: the epilogue computes it
+    if (a.mode == kModeVerify && ri.t < ri.kb && !a.fused) {  // fused: the epilogue computes it
       const int d = a.tokens[static_cast<int64_t>(ri.b) * a.K + ri.t];
       if (d < 0 || d >= a.V) {
         flags |= kFlagToken;
@@ -1967,9 +2013,6 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 // cuts, records the row and -- for the last row of a sequence to finish, found
 // by a counter -- runs the sequence's accept tests and final draw.
 
-__device__ __forceinline__ int fast_div(int n, uint32_t m, uint32_t s) {
-  return static_cast<int>((__umulhi(static_cast<uint32_t>(n), m) + static_cast<uint32_t>(n)) >> s);
-}
 
 // Source of an item: row = item / nseg, then the row's place (decode_job's
 // mapping) with the divisions done by multiply-high.
@@ -1980,10 +2023,11 @@ __device__ __forceinline__ const E* item_src(const KArgs& a, int item, int* s0, 
   int64_t off;
   bool tgt;
   if (a.mode == kModeVerify) {
-    const int b = fast_div(row, a.rows_m, a.rows_s), r = row - b * a.R;
-    tgt = r <= a.K;
+    const SeqRows q = seq_of_row(a, row);
+    const int b = q.b, r = row - q.first;
+    tgt = r <= q.kb;
     off = tgt ? static_cast<int64_t>(b) * a.tgt_seq + static_cast<int64_t>(r) * a.tgt_row
-              : static_cast<int64_t>(b) * a.drf_seq + static_cast<int64_t>(r - (a.K + 1)) * a.drf_row;
+              : static_cast<int64_t>(b) * a.drf_seq + static_cast<int64_t>(r - (q.kb + 1)) * a.drf_row;
   } else {
     const int b = fast_div(row, a.rows_m, a.rows_s), t = row - b * a.K;
     tgt = false;
@@ -2338,7 +2382,7 @@ __global__ void __launch_bounds__(kThreads) spec_row_kernel(const KArgs a) {
       if (threadIdx.x == 0) {
         fence_acq_rel_gpu();
         unsigned long long* tk = &a.tickets[ri.b];
-        const bool last = atomicAdd(tk, 1ull) == static_cast<unsigned long long>(a.R - 1);
+        const bool last = atomicAdd(tk, 1ull) == static_cast<unsigned long long>(ri.nr - 1);
         if (last) {
           *tk = 0ull;  // the sequence's last row: no other arrival of this call
           fence_acq_rel_gpu();
@@ -2346,7 +2390,7 @@ __global__ void __launch_bounds__(kThreads) spec_row_kernel(const KArgs a) {
         sm.bi[15] = last ? 1 : 0;
       }
       __syncthreads();
-      if (sm.bi[15]) verify_epilogue<E>(a, ri.b, sm);
+      if (sm.bi[15]) verify_epilogue<E>(a, ri.b, ri.kb, ri.first, sm);
     }
     __syncthreads();
   }
@@ -2644,6 +2688,72 @@ spec_status spec_verify(const void* target_logits, const void* draft_logits, con
   a.out_n = out_num_accepted;
   a.mode = kModeVerify;
   a.aligned = al ? 1 : 0;
+  fill_common(p, pl, a);
+  fill_rows_div(a);
+  return launch(p, pl, a, di);
+}
+
+size_t spec_verify_ragged_workspace_size(const spec_params* params) {
+  Plan pl;
+  if (make_plan(params, true, &pl) != SPEC_OK) return 0;
+  return pl.ws_bytes + round_up((static_cast<size_t>(params->B) + 1) * sizeof(int32_t), 256);
+}
+
+spec_status spec_verify_ragged(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                               const double* uniforms, const int32_t* draft_lengths, const spec_params* params,
+                               int32_t* out_tokens, int32_t* out_num_accepted) {
+  Plan pl;
+  spec_status s = make_plan(params, true, &pl);
+  if (s != SPEC_OK) return s;
+  const spec_params* p = params;
+  if (p->B == 0) return SPEC_OK;
+  if (!draft_lengths || !target_logits || !draft_tokens || !out_tokens || !out_num_accepted)
+    return SPEC_ERR_INVALID_ARG;
+  if (!p->greedy && (!draft_logits || !uniforms)) return SPEC_ERR_INVALID_ARG;
+  // the rows of every sequence, from its draft length (host array)
+  std::vector<int32_t> start(static_cast<size_t>(p->B) + 1);
+  int64_t total = 0;
+  for (int b = 0; b < p->B; ++b) {
+    const int kb = draft_lengths[b];
+    if (kb < 1 || kb > p->K) return SPEC_ERR_INVALID_ARG;
+    start[b] = static_cast<int32_t>(total);
+    total += p->greedy ? kb + 1 : 2 * kb + 1;
+  }
+  start[p->B] = static_cast<int32_t>(total);
+  const size_t off_start = pl.ws_bytes;
+  const size_t need = off_start + round_up((static_cast<size_t>(p->B) + 1) * sizeof(int32_t), 256);
+  if (!p->workspace || (reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0 || p->workspace_bytes < need)
+    return SPEC_ERR_INVALID_ARG;
+  pl.nrows = total;  // <= the padded B (2K+1) the workspace was sized for
+  pl.items = total * pl.nseg;
+  DevInfo* di = nullptr;
+  if (!dev_info(&di)) return SPEC_ERR_CUDA;
+  s = plan_launch(p, *di, &pl);
+  if (s != SPEC_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(p->stream);
+  int32_t* d_start = reinterpret_cast<int32_t*>(static_cast<char*>(p->workspace) + off_start);
+  // pageable source: the copy is staged before this call returns
+  if (cudaMemcpyAsync(d_start, start.data(), start.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  const int64_t es = pl.esize;
+  bool al = aligned16(target_logits) && (p->target_seq_stride * es) % 16 == 0 && (p->target_row_stride * es) % 16 == 0;
+  if (!p->greedy)
+    al = al && aligned16(draft_logits) && (p->draft_seq_stride * es) % 16 == 0 && (p->draft_row_stride * es) % 16 == 0;
+  KArgs a = {};
+  a.tgt = target_logits;
+  a.drf = draft_logits;
+  a.tgt_seq = p->target_seq_stride;
+  a.tgt_row = p->target_row_stride;
+  a.drf_seq = p->draft_seq_stride;
+  a.drf_row = p->draft_row_stride;
+  a.tokens = draft_tokens;
+  a.u = uniforms;
+  a.out_tokens = out_tokens;
+  a.out_n = out_num_accepted;
+  a.mode = kModeVerify;
+  a.aligned = al ? 1 : 0;
+  a.row_start = d_start;
   fill_common(p, pl, a);
   fill_rows_div(a);
   return launch(p, pl, a, di);

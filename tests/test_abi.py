@@ -128,3 +128,24 @@ def test_sample_verify_requires_k1_sampling_on_the_host(L):
     assert call(ptrs=[fake, fake, fake, fake, None, fake, fake]) == 1   # draft-token output missing
     assert call(B=0) == 0
     assert L.spec_sample_verify(None, None, None, None, None, None, None, None) == 1
+
+
+def test_ragged_lengths_are_checked_on_the_host(L):
+    from speculative_sampling_verification_spec_gb300 import binding as b
+    P = b.SpecParams
+    good = dict(B=3, K=4, V=16, dtype=b.SPEC_F32, target_seq_stride=80, target_row_stride=16,
+                draft_seq_stride=64, draft_row_stride=16, temperature=1.0, top_k=0, top_p=1.0,
+                greedy=0, stream=None, status=None, workspace=0x100000, workspace_bytes=1 << 40)
+    p = P(*[good[f] for f, _ in P._fields_])
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+
+    def call(lens):
+        arr = (ctypes.c_int32 * 3)(*lens) if lens is not None else None
+        return L.spec_verify_ragged(fake, fake, fake, fake, arr, ctypes.byref(p), fake, fake)
+
+    assert call([1, 0, 4]) == 1      # a length below 1
+    assert call([1, 5, 4]) == 1      # a length above K
+    assert call(None) == 1           # no lengths
+    # the ragged workspace holds the padded call's plus the rows' index
+    pv = P(*[dict(good, workspace=None, workspace_bytes=0)[f] for f, _ in P._fields_])
+    assert L.spec_verify_ragged_workspace_size(ctypes.byref(pv)) > L.spec_verify_workspace_size(ctypes.byref(pv))

@@ -339,3 +339,35 @@ def test_sample_verify_equals_draw_then_verify(sv, name, kw, prm):
     torch.cuda.synchronize()
     assert np.array_equal(s_d.cpu().numpy()[:, 0], g_d)
     assert np.array_equal(s_n.cpu().numpy(), g_n) and np.array_equal(s_t.cpu().numpy(), g_t)
+
+
+@pytest.mark.parametrize("name,kw,prm", [
+    ("c3", dict(B=24, V=30011), {}),
+    ("c5", dict(B=12), {}),
+    ("c4", dict(B=40, V=20011), {}),
+    ("c1", dict(B=300), dict(top_k=6, top_p=0.85))])
+def test_ragged_batch_equals_per_sequence_verify(sv, name, kw, prm):
+    """Each sequence of a ragged call gives the oracle's verification with its own
+    draft length K_b: the first K_b draft tokens, uniform columns 0..K_b."""
+    w = workloads.make(name, **kw)
+    p = dict(params_of(w), **prm)
+    B, K = w["B"], w["K"]
+    rng = np.random.default_rng(40 + K)
+    lens = rng.integers(1, K + 1, B).astype(np.int32)
+    lens[0] = K
+    d = oracle.sample_draft(w["draft"], w["u_draft"], **p)["tokens"]
+    g_t, g_n = sv.spec_verify_ragged(to_dev(w["target"]), to_dev(w["draft"]), to_dev(d),
+                                     None if p["greedy"] else to_dev(w["u_verify"]), lens, **p)
+    torch.cuda.synchronize()
+    g_t, g_n = g_t.cpu().numpy(), g_n.cpu().numpy()
+    compared = 0
+    for kb in sorted(set(lens.tolist())):
+        sel = np.nonzero(lens == kb)[0]
+        ref = oracle.verify(np.ascontiguousarray(w["target"][sel, :kb + 1]), np.ascontiguousarray(w["draft"][sel, :kb]),
+                            np.ascontiguousarray(d[sel, :kb]), np.ascontiguousarray(w["u_verify"][sel, :kb + 1]), **p)
+        ok = ref["flags"] == 0
+        assert np.array_equal(g_n[sel][ok], ref["num_accepted"][ok]), kb
+        assert np.array_equal(g_t[sel][ok][:, :kb + 1], ref["tokens"][ok]), kb
+        assert np.all(g_t[sel][:, kb + 1:] == -1)
+        compared += int(ok.sum())
+    assert compared >= 0.9 * B
