@@ -328,7 +328,7 @@ struct KArgs {
   int fused;            // verify with K = 1 whose draft token is drawn in the same call
   const double* u_draft;  // fused: [B] uniforms of the draft draws
   int32_t* out_draft;     // fused: [B] the drawn draft tokens (tokens aliases it)
-  const int32_t* row_start;  // ragged verify: [B + 1] first row of each sequence (NULL: R rows each)
+  const int2* row_map;  // ragged verify: [nrows] {sequence, position | K_b << 16} (NULL: R rows each)
   int need_z;           // segments sum the normaliser (no filter, or top-p without top-k)
   int filt, n0;         // segments list candidates; theta is the n0-th thread maximum
   float top_p, c, temp;
@@ -1195,24 +1195,21 @@ __device__ __forceinline__ int fast_div(int n, uint32_t m, uint32_t s) {
   return static_cast<int>((__umulhi(static_cast<uint32_t>(n), m) + static_cast<uint32_t>(n)) >> s);
 }
 
-// Ragged verification: the sequence of a row, by binary search in the prefix
-// of rows per sequence (row_start[b] <= row < row_start[b + 1]); its rows are
-// its K_b + 1 target rows, then (sampling) its K_b draft rows.
+// The sequence of a verify row: R rows per sequence, or (ragged calls) the
+// host's per-row table {b, position | K_b << 16}; a sequence's rows are its
+// K_b + 1 target rows, then (sampling) its K_b draft rows.
 struct SeqRows {
   int b, first, nr, kb;
 };
+template <bool RAG>
 __device__ __forceinline__ SeqRows seq_of_row(const KArgs& a, int row) {
   SeqRows q;
-  if (a.row_start) {
-    int lo = 0, hi = a.B;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(&a.row_start[mid]) <= row) lo = mid; else hi = mid;
-    }
-    q.b = lo;
-    q.first = __ldg(&a.row_start[lo]);
-    q.nr = __ldg(&a.row_start[lo + 1]) - q.first;
-    q.kb = a.greedy ? q.nr - 1 : (q.nr - 1) >> 1;
+  if constexpr (RAG) {
+    const int2 e = __ldg(&a.row_map[row]);
+    q.b = e.x;
+    q.kb = e.y >> 16;
+    q.first = row - (e.y & 0xffff);
+    q.nr = a.greedy ? q.kb + 1 : 2 * q.kb + 1;
   } else {
     q.b = fast_div(row, a.rows_m, a.rows_s);
     q.first = q.b * a.R;
@@ -1222,12 +1219,13 @@ __device__ __forceinline__ SeqRows seq_of_row(const KArgs& a, int row) {
   return q;
 }
 
+template <bool RAG>
 __device__ RowInfo decode_job(const KArgs& a, int job) {
   RowInfo ri;
   ri.job = job;
   ri.tok = -1;
   if (a.mode == kModeVerify) {
-    const SeqRows q = seq_of_row(a, job);
+    const SeqRows q = seq_of_row<RAG>(a, job);
     ri.b = q.b;
     ri.kb = q.kb;
     ri.first = q.first;
@@ -1338,6 +1336,24 @@ __device__ int global_rows_draw(const KArgs& a, const E* gt, const E* gd, float 
 // ---------------------------------------------------------------------------
 // verify epilogue: the rank-0 CTA of the last cluster of sequence b
 
+// Accept test of a fused call's draft token d (K = 1): the token was drawn by
+// the draft row of the same call, so its probabilities under both adjusted
+// rows are computed here, with the arithmetic of the row records.
+template <typename E>
+__device__ __noinline__ bool fused_accept(const KArgs& a, int b, int d, const spec_row_stat& rt,
+                                          const spec_row_stat& rd, double u) {
+  const E* gt = static_cast<const E*>(a.tgt) + static_cast<int64_t>(b) * a.tgt_seq;
+  const E* gd = static_cast<const E*>(a.drf) + static_cast<int64_t>(b) * a.drf_seq;
+  auto prob = [&](const E* g, const spec_row_stat& r) -> double {
+    if (d < 0 || d >= a.V) return 0.0;
+    const float l = Fmt<E>::at_global(g, d);
+    const Cut c{__ldcg(&r.tau_val), __ldcg(&r.tau_idx)};
+    if (!(c.keep(l, d) && l > -INFINITY)) return 0.0;
+    return static_cast<double>(wexp(l, __ldcg(&r.m), a.c)) / __ldcg(&r.zf);
+  };
+  return u * prob(gd, rd) < prob(gt, rt);
+}
+
 template <typename E>
 // K = this sequence's draft length (ragged: K_b <= a.K); token, uniform and
 // output arrays keep the call's strides (a.K, a.K + 1), and the final draw
@@ -1361,20 +1377,7 @@ __device__ void verify_epilogue(const KArgs& a, int b, int K, int first, Scratch
       if (a.greedy) {
         acc = (d == __ldcg(&recs[t].argmax));
       } else if (a.fused) {
-        // the token was drawn by the draft row of this call: its probabilities
-        // under both adjusted rows, with the arithmetic of the row records
-        const E* gt = static_cast<const E*>(a.tgt) + static_cast<int64_t>(b) * a.tgt_seq;
-        const E* gd = static_cast<const E*>(a.drf) + static_cast<int64_t>(b) * a.drf_seq;
-        auto prob = [&](const E* g, const spec_row_stat& r) -> double {
-          if (d < 0 || d >= a.V) return 0.0;
-          const float l = Fmt<E>::at_global(g, d);
-          const Cut c{__ldcg(&r.tau_val), __ldcg(&r.tau_idx)};
-          if (!(c.keep(l, d) && l > -INFINITY)) return 0.0;
-          return static_cast<double>(wexp(l, __ldcg(&r.m), a.c)) / __ldcg(&r.zf);
-        };
-        const double pt = prob(gt, recs[t]);
-        const double pd = prob(gd, recs[K + 1 + t]);
-        acc = a.u[static_cast<int64_t>(b) * (KS + 1) + t] * pd < pt;
+        acc = fused_accept<E>(a, b, d, recs[t], recs[K + 1 + t], a.u[static_cast<int64_t>(b) * (KS + 1) + t]);
       } else {
         // keep d_t with probability min(1, tgt/drf):  u * drf < tgt
         const double pt = __ldcg(&recs[t].p_tok);
@@ -2016,14 +2019,14 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 
 // Source of an item: row = item / nseg, then the row's place (decode_job's
 // mapping) with the divisions done by multiply-high.
-template <typename E>
+template <typename E, bool RAG>
 __device__ __forceinline__ const E* item_src(const KArgs& a, int item, int* s0, int* L) {
   const int row = fast_div(item, a.nseg_m, a.nseg_s);
   const int seg = item - row * a.nseg;
   int64_t off;
   bool tgt;
   if (a.mode == kModeVerify) {
-    const SeqRows q = seq_of_row(a, row);
+    const SeqRows q = seq_of_row<RAG>(a, row);
     const int b = q.b, r = row - q.first;
     tgt = r <= q.kb;
     off = tgt ? static_cast<int64_t>(b) * a.tgt_seq + static_cast<int64_t>(r) * a.tgt_row
@@ -2041,10 +2044,10 @@ __device__ __forceinline__ const E* item_src(const KArgs& a, int item, int* s0, 
 // Thread 0: start the bulk copy of an item's 16-byte-aligned part into a
 // segment buffer (one arrival with its byte count; a zero count completes the
 // phase at once).
-template <typename E>
+template <typename E, bool RAG>
 __device__ __forceinline__ void item_issue(const KArgs& a, int item, void* segbuf, uint64_t* bar) {
   int s0, L;
-  const E* g = item_src<E>(a, item, &s0, &L);
+  const E* g = item_src<E, RAG>(a, item, &s0, &L);
   const uint32_t bytes = static_cast<uint32_t>(L) * sizeof(E) & ~15u;
   mbar_expect_tx(bar, bytes);
   if (bytes > 0) bulk_copy_g2s(segbuf, g, bytes, bar);
@@ -2064,7 +2067,8 @@ __device__ __forceinline__ uint4 item_vec(const E* g, int L, bool staged, bool a
   return Seg<E>::neg_inf();
 }
 
-template <typename E>
+// RAG: a ragged call (rows found through the host's per-row table)
+template <typename E, bool RAG>
 __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
@@ -2100,8 +2104,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
     issued0 = beg < end;
     issued1 = beg + 1 < end;
     if (tid == 0) {
-      if (issued0) item_issue<E>(a, beg, bufs, &sm.bar[0]);
-      if (issued1) item_issue<E>(a, beg + 1, bufs + a.seg_bytes, &sm.bar[1]);
+      if (issued0) item_issue<E, RAG>(a, beg, bufs, &sm.bar[0]);
+      if (issued1) item_issue<E, RAG>(a, beg + 1, bufs + a.seg_bytes, &sm.bar[1]);
     }
   }
 
@@ -2113,7 +2117,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
     prev_row = row;
     const bool run_ends = cur + 1 >= end || fast_div(cur + 1, a.nseg_m, a.nseg_s) != row;
     int s0, L;
-    const E* g = item_src<E>(a, cur, &s0, &L);
+    const E* g = item_src<E, RAG>(a, cur, &s0, &L);
     const uint4* seg = reinterpret_cast<const uint4*>(bufs + p * a.seg_bytes);
 
     // ---- wait for this item's copy
@@ -2330,7 +2334,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
     if (p) issued1 = refill; else issued0 = refill;
     if (tid == 0 && refill) {
       fence_proxy_async_smem();
-      item_issue<E>(a, nxt, bufs + p * a.seg_bytes, &sm.bar[p]);
+      item_issue<E, RAG>(a, nxt, bufs + p * a.seg_bytes, &sm.bar[p]);
     }
 
     // ---- the segment record (thread 0)
@@ -2360,8 +2364,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
 }
 
 // Row merge, cut, record and (verify) the sequence counter and epilogue.
-template <typename E>
-__global__ void __launch_bounds__(kThreads) spec_row_kernel(const KArgs a) {
+template <typename E, bool RAG>
+__global__ void __launch_bounds__(kThreads, 5) spec_row_kernel(const KArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
   unsigned char* scratch = smem_raw + sizeof(Scratch);
@@ -2372,7 +2376,7 @@ __global__ void __launch_bounds__(kThreads) spec_row_kernel(const KArgs a) {
   // grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int row = static_cast<int>(blockIdx.x); row < a.nrows; row += static_cast<int>(gridDim.x)) {
-    const RowInfo ri = decode_job(a, row);
+    const RowInfo ri = decode_job<RAG>(a, row);
     const E* grow = static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off;
     Local C;
     row_finish<E>(a, ri, grow, sm, C, sb, pool_idx, pool_val);
@@ -2428,8 +2432,8 @@ std::atomic<uint64_t> g_launches{0};
 struct DevInfo {
   int sms = 0;
   int max_smem = 0;
-  size_t smem_set[4] = {0, 0, 0, 0};  // dynamic smem attribute set: [kernel * 2 + dtype]
-  int per_sm[2] = {0, 0};              // resident segment-kernel CTAs per SM, per dtype
+  size_t smem_set[8] = {};  // dynamic smem attribute set: [kernel * 4 + ragged * 2 + dtype]
+  int per_sm[4] = {};       // resident segment-kernel CTAs per SM: [ragged * 2 + dtype]
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
@@ -2453,6 +2457,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Plan {
   int esize = 0, R = 0, S = 0, nseg = 0, n0 = 0, grid = 0, row_grid = 0, seg_bytes = 0;
   bool clear_counters = false;  // more counters than the area that calls keep zeroed
+  bool ragged = false;          // per-sequence draft lengths (the kernels' RAG instantiation)
   size_t counter_bytes = 0;
   int64_t nrows = 0, items = 0;
   size_t smem = 0, row_smem = 0;  // dynamic shared memory of the segment and row kernels
@@ -2521,9 +2526,15 @@ spec_status make_plan(const spec_params* p, bool verify, Plan* pl) {
 }
 
 template <typename E>
-const void* seg_fn() { return reinterpret_cast<const void*>(&spec_seg_kernel<E>); }
+const void* seg_fn(bool rag) {
+  return rag ? reinterpret_cast<const void*>(&spec_seg_kernel<E, true>)
+             : reinterpret_cast<const void*>(&spec_seg_kernel<E, false>);
+}
 template <typename E>
-const void* row_fn() { return reinterpret_cast<const void*>(&spec_row_kernel<E>); }
+const void* row_fn(bool rag) {
+  return rag ? reinterpret_cast<const void*>(&spec_row_kernel<E, true>)
+             : reinterpret_cast<const void*>(&spec_row_kernel<E, false>);
+}
 
 spec_status set_smem(DevInfo& di, int slot, const void* fn, size_t bytes) {
   if (di.smem_set[slot] >= bytes) return SPEC_OK;
@@ -2540,21 +2551,23 @@ spec_status plan_launch(const spec_params* p, DevInfo& di, Plan* pl) {
   if (pl->smem > static_cast<size_t>(di.max_smem) || pl->row_smem > static_cast<size_t>(di.max_smem))
     return SPEC_ERR_UNSUPPORTED;
   const int which = (p->dtype == SPEC_F32) ? 0 : 1;
-  const void* fs = which == 0 ? seg_fn<float>() : seg_fn<uint16_t>();
-  const void* fr = which == 0 ? row_fn<float>() : row_fn<uint16_t>();
+  const bool rag = pl->ragged;
+  const void* fs = which == 0 ? seg_fn<float>(rag) : seg_fn<uint16_t>(rag);
+  const void* fr = which == 0 ? row_fn<float>(rag) : row_fn<uint16_t>(rag);
+  const int slot = (rag ? 2 : 0) + which;
   std::lock_guard<std::mutex> lock(g_mu);
-  const size_t before = di.smem_set[which];
-  spec_status s = set_smem(di, which, fs, pl->smem);
+  const size_t before = di.smem_set[slot];
+  spec_status s = set_smem(di, slot, fs, pl->smem);
   if (s != SPEC_OK) return s;
-  s = set_smem(di, 2 + which, fr, pl->row_smem);
+  s = set_smem(di, 4 + slot, fr, pl->row_smem);
   if (s != SPEC_OK) return s;
-  if (di.per_sm[which] == 0 || di.smem_set[which] != before) {
+  if (di.per_sm[slot] == 0 || di.smem_set[slot] != before) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fs, kThreads, pl->smem) != cudaSuccess || per_sm < 1)
       return SPEC_ERR_CUDA;
-    di.per_sm[which] = per_sm;
+    di.per_sm[slot] = per_sm;
   }
-  pl->grid = static_cast<int>(std::min<int64_t>(pl->items, static_cast<int64_t>(di.per_sm[which]) * di.sms));
+  pl->grid = static_cast<int>(std::min<int64_t>(pl->items, static_cast<int64_t>(di.per_sm[slot]) * di.sms));
   pl->row_grid = static_cast<int>(std::min<int64_t>(pl->nrows, int64_t(1) << 20));
   return SPEC_OK;
 }
@@ -2581,12 +2594,18 @@ spec_status launch(const spec_params* p, const Plan& pl, KArgs& a, DevInfo* di) 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (p->dtype == SPEC_F32) {
-    spec_seg_kernel<float><<<grid, block, pl.smem, st>>>(a);
-    e = cudaLaunchKernelEx(&cfg, spec_row_kernel<float>, a);
+  if (p->dtype == SPEC_F32 && !pl.ragged) {
+    spec_seg_kernel<float, false><<<grid, block, pl.smem, st>>>(a);
+    e = cudaLaunchKernelEx(&cfg, spec_row_kernel<float, false>, a);
+  } else if (p->dtype == SPEC_F32) {
+    spec_seg_kernel<float, true><<<grid, block, pl.smem, st>>>(a);
+    e = cudaLaunchKernelEx(&cfg, spec_row_kernel<float, true>, a);
+  } else if (!pl.ragged) {
+    spec_seg_kernel<uint16_t, false><<<grid, block, pl.smem, st>>>(a);
+    e = cudaLaunchKernelEx(&cfg, spec_row_kernel<uint16_t, false>, a);
   } else {
-    spec_seg_kernel<uint16_t><<<grid, block, pl.smem, st>>>(a);
-    e = cudaLaunchKernelEx(&cfg, spec_row_kernel<uint16_t>, a);
+    spec_seg_kernel<uint16_t, true><<<grid, block, pl.smem, st>>>(a);
+    e = cudaLaunchKernelEx(&cfg, spec_row_kernel<uint16_t, true>, a);
   }
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   g_launches.fetch_add(2, std::memory_order_relaxed);
@@ -2696,7 +2715,7 @@ spec_status spec_verify(const void* target_logits, const void* draft_logits, con
 size_t spec_verify_ragged_workspace_size(const spec_params* params) {
   Plan pl;
   if (make_plan(params, true, &pl) != SPEC_OK) return 0;
-  return pl.ws_bytes + round_up((static_cast<size_t>(params->B) + 1) * sizeof(int32_t), 256);
+  return pl.ws_bytes + round_up(static_cast<size_t>(pl.nrows) * sizeof(int2), 256);
 }
 
 spec_status spec_verify_ragged(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
@@ -2710,31 +2729,33 @@ spec_status spec_verify_ragged(const void* target_logits, const void* draft_logi
   if (!draft_lengths || !target_logits || !draft_tokens || !out_tokens || !out_num_accepted)
     return SPEC_ERR_INVALID_ARG;
   if (!p->greedy && (!draft_logits || !uniforms)) return SPEC_ERR_INVALID_ARG;
-  // the rows of every sequence, from its draft length (host array)
-  std::vector<int32_t> start(static_cast<size_t>(p->B) + 1);
-  int64_t total = 0;
+  // the rows of every sequence, from its draft length (host array): one
+  // {sequence, position | K_b << 16} entry per row
+  if (p->K >= 32768) return SPEC_ERR_UNSUPPORTED;
+  std::vector<int2> map;
+  map.reserve(static_cast<size_t>(pl.nrows));
   for (int b = 0; b < p->B; ++b) {
     const int kb = draft_lengths[b];
     if (kb < 1 || kb > p->K) return SPEC_ERR_INVALID_ARG;
-    start[b] = static_cast<int32_t>(total);
-    total += p->greedy ? kb + 1 : 2 * kb + 1;
+    const int nr = p->greedy ? kb + 1 : 2 * kb + 1;
+    for (int r = 0; r < nr; ++r) map.push_back(make_int2(b, r | (kb << 16)));
   }
-  start[p->B] = static_cast<int32_t>(total);
+  const int64_t total = static_cast<int64_t>(map.size());
   const size_t off_start = pl.ws_bytes;
-  const size_t need = off_start + round_up((static_cast<size_t>(p->B) + 1) * sizeof(int32_t), 256);
+  const size_t need = off_start + round_up(static_cast<size_t>(pl.nrows) * sizeof(int2), 256);
   if (!p->workspace || (reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0 || p->workspace_bytes < need)
     return SPEC_ERR_INVALID_ARG;
   pl.nrows = total;  // <= the padded B (2K+1) the workspace was sized for
+  pl.ragged = true;
   pl.items = total * pl.nseg;
   DevInfo* di = nullptr;
   if (!dev_info(&di)) return SPEC_ERR_CUDA;
   s = plan_launch(p, *di, &pl);
   if (s != SPEC_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(p->stream);
-  int32_t* d_start = reinterpret_cast<int32_t*>(static_cast<char*>(p->workspace) + off_start);
+  int2* d_map = reinterpret_cast<int2*>(static_cast<char*>(p->workspace) + off_start);
   // pageable source: the copy is staged before this call returns
-  if (cudaMemcpyAsync(d_start, start.data(), start.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st) !=
-      cudaSuccess)
+  if (cudaMemcpyAsync(d_map, map.data(), map.size() * sizeof(int2), cudaMemcpyHostToDevice, st) != cudaSuccess)
     return SPEC_ERR_CUDA;
   const int64_t es = pl.esize;
   bool al = aligned16(target_logits) && (p->target_seq_stride * es) % 16 == 0 && (p->target_row_stride * es) % 16 == 0;
@@ -2753,7 +2774,7 @@ spec_status spec_verify_ragged(const void* target_logits, const void* draft_logi
   a.out_n = out_num_accepted;
   a.mode = kModeVerify;
   a.aligned = al ? 1 : 0;
-  a.row_start = d_start;
+  a.row_map = d_map;
   fill_common(p, pl, a);
   fill_rows_div(a);
   return launch(p, pl, a, di);
