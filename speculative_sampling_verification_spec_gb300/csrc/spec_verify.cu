@@ -2364,8 +2364,11 @@ __global__ void __launch_bounds__(kThreads, 4) spec_seg_kernel(const KArgs a) {
 }
 
 // Row merge, cut, record and (verify) the sequence counter and epilogue.
+// At most 102 registers (5 CTAs per SM; bf16 rows need that many without
+// spilling), fp32 rows 64 (8 per SM: the 1024 rows of a greedy batch of 256
+// sequences run in one wave; ptxas moves a few values to the stack).
 template <typename E, bool RAG>
-__global__ void __launch_bounds__(kThreads, 5) spec_row_kernel(const KArgs a) {
+__global__ void __launch_bounds__(kThreads, sizeof(E) == 4 ? 8 : 5) spec_row_kernel(const KArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
   unsigned char* scratch = smem_raw + sizeof(Scratch);
