@@ -371,3 +371,19 @@ def test_ragged_batch_equals_per_sequence_verify(sv, name, kw, prm):
         assert np.all(g_t[sel][:, kb + 1:] == -1)
         compared += int(ok.sum())
     assert compared >= 0.9 * B
+
+
+@pytest.mark.parametrize("name,kw", [("c5", dict(B=6)), ("c4", dict(B=20, V=20011)), ("c3", dict(B=8, V=30011)),
+                                     ("c2", {})])
+def test_ragged_with_equal_lengths_is_spec_verify(sv, name, kw):
+    """A ragged call whose lengths all equal K gives spec_verify's outputs bit for bit."""
+    w = workloads.make(name, **kw)
+    p = params_of(w)
+    d = to_dev(oracle.sample_draft(w["draft"], w["u_draft"], **p)["tokens"])
+    tgt, drf = to_dev(w["target"]), to_dev(w["draft"])
+    u = None if p["greedy"] else to_dev(w["u_verify"])
+    a_t, a_n = sv.spec_verify(tgt, drf, d, u, **p)
+    b_t, b_n = sv.spec_verify_ragged(tgt, drf, d, u, np.full(w["B"], w["K"], np.int32), **p)
+    torch.cuda.synchronize()
+    assert np.array_equal(a_t.cpu().numpy(), b_t.cpu().numpy())
+    assert np.array_equal(a_n.cpu().numpy(), b_n.cpu().numpy())
