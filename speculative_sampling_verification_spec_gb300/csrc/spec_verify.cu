@@ -625,16 +625,6 @@ __device__ __forceinline__ void sort_stage_lanes(unsigned long long (&key)[R], i
   }
 }
 
-// 32 R keys in one warp.
-template <int R>
-__device__ void warp_sort_keys_desc(unsigned long long (&key)[R], int lane) {
-  for (int k = 2; k <= 32 * R; k <<= 1)
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j < R) sort_stage_regs<R>(key, lane, k, j);
-      else sort_stage_lanes<R>(key, lane, k, j);
-    }
-}
-
 // kThreads * R keys over the whole block; xbuf holds kThreads * R keys.
 template <int R>
 __device__ void block_sort_keys_desc(unsigned long long (&key)[R], unsigned long long* xbuf) {
