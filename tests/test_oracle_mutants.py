@@ -37,6 +37,8 @@ MUTANTS = {
                          "if (isinf(l[x]) && l[x] > 0) status = ORACLE_ERR_NONFINITE;"),
     "residual_uses_next_row": ("const double* pd = P + (size_t)(nt + n) * V;",
                                "const double* pd = P + (size_t)(nt + (n + 1 < K ? n + 1 : n)) * V;"),
+    "histogram_drops_all_accepted": ("if (n >= 0 && n <= K)", "if (n >= 0 && n < K)"),
+    "histogram_bins_off_by_one": ("hist[n] += 1;", "hist[n > 0 ? n - 1 : 0] += 1;"),
 }
 
 
