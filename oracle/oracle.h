@@ -27,7 +27,7 @@
  *   - drawing draft tokens from the adjusted draft distribution
  *     ("Speculative Decoding", section "Draft, then verify", step 1).
  *
- * Readings where the pages are silent (each listed in the design doc):
+ * Readings where the pages are silent (the CUDA library takes the same ones):
  *   accept test written as  u * drf < tgt  (no division; drf = 0 accepts iff
  *   tgt > 0); inverse-CDF draws walk the vocabulary in ascending index order
  *   and pick the smallest x with  u * R < cumsum(x);  if rounding leaves no

@@ -436,3 +436,166 @@ def test_sample_draft_is_categorical_by_library_routine():
                 assert res["tokens"][b, t] == want
     g = oracle.sample_draft(dl, None, greedy=True)
     np.testing.assert_array_equal(g["tokens"], np.argmax(dl, axis=-1))
+
+
+# --------------------------------------------------------------------------
+# near-threshold flags: the only exclusions from bit-exact GPU parity.  A
+# decision is flagged when its uniform (or, for top-p, the cumulative mass at
+# the cut) lies within 1e-6 of the threshold it is compared with ("within
+# hardware numerics": paperlayer.ai summary of "Accelerating Large Language
+# Model Decoding with Speculative Sampling", abstract; the thresholds are those
+# of "Speculative Decoding", roadtointelligence.com, "Draft, then verify",
+# steps 3-4).  Each pin places the uniform or top_p at a known distance from a
+# threshold computed independently with numpy in fp64: 0.5e-6 must flag, 2e-6
+# and 5e-6 must not, and the decision itself must fall on the right side.
+
+EPS = 1e-6
+INSIDE, OUTSIDE = 0.5e-6, (2e-6, 5e-6)
+
+
+def _np_probs(row, T=1.0):
+    """Softmax of fp32 logits in fp64 (numpy), the reference for the thresholds."""
+    return _softmax_numpy(np.asarray(row, np.float32), T)
+
+
+def _flag_rows(seed=41, V=6):
+    """One K=1 sequence: target rows 0 and 1, draft row 0 (fp32 logits)."""
+    rng = np.random.default_rng(seed)
+    tl = rng.normal(0, 1.2, (2, V)).astype(np.float32)
+    dl = (tl[:1] + rng.normal(0, 1.2, (1, V))).astype(np.float32)
+    return tl, dl
+
+
+def _verify_one(tl, dl, d, u, **kw):
+    res = oracle.verify(tl[None], dl[None], np.asarray([d], np.int32), np.asarray([u], np.float64), **kw)
+    assert res["status"] == oracle.OK
+    return int(res["num_accepted"][0]), res["tokens"][0], int(res["flags"][0])
+
+
+def test_near_flag_accept_band():
+    tl, dl = _flag_rows()
+    tp, dp = _np_probs(tl[0]), _np_probs(dl[0])
+    # a token the draft over-weights, with a small draft probability, so that a
+    # band scaled by drf (|u drf - tgt| instead of |u - tgt/drf|) would be wider
+    cand = [x for x in range(len(tp)) if tp[x] < dp[x] and dp[x] < 0.45]
+    assert cand
+    x = cand[0]
+    ratio = tp[x] / dp[x]
+    for off in (INSIDE, *OUTSIDE):
+        for sign in (-1, 1):
+            u0 = ratio + sign * off
+            n, _, fl = _verify_one(tl, dl, [x], [u0, 0.37])
+            assert n == (1 if sign < 0 else 0), (off, sign)          # accept iff u < ratio
+            assert bool(fl & oracle.NEAR_ACCEPT) == (off < EPS), (off, sign, fl)
+
+
+def test_near_flag_accept_only_for_tests_taken():
+    rng = np.random.default_rng(43)
+    V, K = 6, 2
+    tl = rng.normal(0, 1.2, (K + 1, V)).astype(np.float32)
+    dl = (tl[:K] + rng.normal(0, 1.2, (K, V))).astype(np.float32)
+    tp = [_np_probs(r) for r in tl]
+    dp = [_np_probs(r) for r in dl]
+    x0 = int(np.argmax(dp[0] - tp[0]))     # tgt < drf at position 0: u near 1 rejects
+    x1 = int(np.argmax(dp[1] - tp[1]))
+    r1 = tp[1][x1] / dp[1][x1]
+    assert tp[0][x0] / dp[0][x0] < 0.99 and r1 < 1
+    # position 0 rejects, so the test at position 1 (u exactly at its ratio) is never taken
+    res = oracle.verify(tl[None], dl[None], np.asarray([[x0, x1]], np.int32),
+                        np.asarray([[1 - 1e-9, r1, 0.41]]))
+    assert res["num_accepted"][0] == 0 and not (res["flags"][0] & oracle.NEAR_ACCEPT)
+    # position 0 accepts (u = 0), so the test at position 1 is taken and flagged
+    res = oracle.verify(tl[None], dl[None], np.asarray([[x0, x1]], np.int32),
+                        np.asarray([[0.0, r1, 0.41]]))
+    assert res["num_accepted"][0] >= 1 and (res["flags"][0] & oracle.NEAR_ACCEPT)
+
+
+def _edges(w, x):
+    """CDF edges cum(x-1)/R and cum(x)/R of token x under weights w (index order)."""
+    c = np.cumsum(w)
+    return (c[x - 1] if x > 0 else 0.0) / c[-1], c[x] / c[-1]
+
+
+def test_near_flag_residual_draw_edges():
+    tl, dl = _flag_rows(seed=47, V=8)
+    tp, dp = _np_probs(tl[0]), _np_probs(dl[0])
+    r = np.maximum(0.0, tp - dp)
+    R = r.sum()
+    assert 0.05 < R < 0.5      # a band scaled by R would be at least twice as wide
+    d = int(np.argmax(dp - tp))
+    pos = [x for x in range(len(r)) if r[x] > 0]
+    x = pos[len(pos) // 2]
+    assert x > pos[0]
+    lo, hi = _edges(r, x)
+    for off in (INSIDE, *OUTSIDE):
+        for u1 in (lo + off, hi - off):
+            n, tok, fl = _verify_one(tl, dl, [d], [1 - 1e-12, u1])
+            assert n == 0 and tok[0] == x, (off, u1)
+            assert bool(fl & oracle.NEAR_DRAW) == (off < EPS), (off, u1, fl)
+
+
+def test_near_flag_bonus_draw_edges():
+    tl, dl = _flag_rows(seed=53, V=8)
+    tp1 = _np_probs(tl[1])
+    d = int(np.argmax(_np_probs(tl[0])))
+    x = 4
+    lo, hi = _edges(tp1, x)
+    for off in (INSIDE, *OUTSIDE):
+        for u1 in (lo + off, hi - off):
+            n, tok, fl = _verify_one(tl, dl, [d], [0.0, u1])
+            assert n == 1 and tok[1] == x, (off, u1)
+            assert bool(fl & oracle.NEAR_DRAW) == (off < EPS), (off, u1, fl)
+
+
+def test_near_flag_sample_draft_edges():
+    rng = np.random.default_rng(59)
+    V = 10
+    row = rng.normal(0, 1.5, (1, 1, V)).astype(np.float32)
+    p = _np_probs(row[0, 0], 0.9)
+    x = 6
+    lo, hi = _edges(p, x)
+    for off in (INSIDE, *OUTSIDE):
+        for u in (lo + off, hi - off):
+            res = oracle.sample_draft(row, np.asarray([[u]]), temperature=0.9)
+            assert res["tokens"][0, 0] == x
+            assert bool(res["flags"][0, 0] & oracle.NEAR_DRAW) == (off < EPS), (off, u)
+
+
+def _crossing_masses(row, T=1.0, top_k=0):
+    """Cumulative masses along (logit desc, index asc), relative to the top-k mass."""
+    lf = np.asarray(row, np.float32)
+    order = _order(lf)
+    w = np.exp((lf[order].astype(np.float64) - lf[order[0]]) / float(np.float32(T)))
+    if top_k:
+        w = w[:top_k]
+    return np.cumsum(w) / w.sum()
+
+
+@pytest.mark.parametrize("top_k,j", [(0, 3), (0, 1), (6, 2)])
+def test_near_flag_top_p_band(top_k, j):
+    rng = np.random.default_rng(61 + j)
+    V = 12
+    row = rng.normal(0, 1.0, V).astype(np.float32)
+    cm = _crossing_masses(row, top_k=top_k)
+    c = cm[j]
+    for off in (INSIDE, *OUTSIDE):
+        for sign in (-1, 1):
+            p32 = np.float32(c + sign * off)
+            dist = abs(c - float(p32))
+            probs, _, near, _, s = oracle.row_probs(row, top_k=top_k, top_p=float(p32))
+            assert s == oracle.OK
+            # kept: the prefix through j when top_p <= c, else through j + 1
+            assert int((probs > 0).sum()) == (j + 1 if float(p32) <= c else j + 2), (off, sign)
+            assert near == (dist < EPS), (off, sign, dist)
+    # the same flag reaches verify's per-sequence bits (NEAR_TOPP) and sample_draft's
+    tl = np.stack([row, row])
+    p32 = float(np.float32(c + INSIDE))
+    res = oracle.verify(tl[None], row[None, None], np.asarray([[0]], np.int32), np.asarray([[0.0, 0.5]]),
+                        top_k=top_k, top_p=p32)
+    assert res["flags"][0] & oracle.NEAR_TOPP
+    sd = oracle.sample_draft(row[None, None], np.asarray([[0.5]]), top_k=top_k, top_p=p32)
+    assert sd["flags"][0, 0] & oracle.NEAR_TOPP
+    p32 = float(np.float32(c + OUTSIDE[1]))
+    res = oracle.verify(tl[None], row[None, None], np.asarray([[0]], np.int32), np.asarray([[0.0, 0.5]]),
+                        top_k=top_k, top_p=p32)
+    assert not (res["flags"][0] & oracle.NEAR_TOPP)

@@ -1,7 +1,8 @@
 """The oracle's pins catch plausible mistakes.
 
-Each case plants one mistake in a temporary copy of oracle/oracle.c (a transposed
-operand, a wrong sign or index, a dropped term), builds it, and runs the pin suite
+Each case plants one mistake in a temporary copy of oracle/oracle.c or oracle/oracle.h
+(a transposed operand, a wrong sign or index, a dropped term, a misplaced or
+mis-sized near-threshold band), builds it, and runs the pin suite
 (tests/test_oracle.py) against it in a subprocess: the suite must fail.  The
 committed oracle is never modified.
 """
@@ -15,7 +16,7 @@ from concurrent.futures import ThreadPoolExecutor
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SRC = os.path.join(ROOT, "oracle", "oracle.c")
+ORACLE_DIR = os.path.join(ROOT, "oracle")
 
 MUTANTS = {
     "accept_operands_transposed": ("if (!(u[t] * b < a)) { n = t; break; }",
@@ -39,17 +40,41 @@ MUTANTS = {
                                "const double* pd = P + (size_t)(nt + (n + 1 < K ? n + 1 : n)) * V;"),
     "histogram_drops_all_accepted": ("if (n >= 0 && n <= K)", "if (n >= 0 && n < K)"),
     "histogram_bins_off_by_one": ("hist[n] += 1;", "hist[n > 0 ? n - 1 : 0] += 1;"),
+    # the near-threshold flags, which decide every exclusion from bit-exact parity
+    "draw_band_scaled_by_R": (
+        "*near = fabs(u - prev / R) < ORACLE_NEAR_EPS || fabs(u - cum / R) < ORACLE_NEAR_EPS;",
+        "*near = fabs(target - prev) < ORACLE_NEAR_EPS || fabs(target - cum) < ORACLE_NEAR_EPS;"),
+    "draw_lower_edge_dropped": (
+        "*near = fabs(u - prev / R) < ORACLE_NEAR_EPS || fabs(u - cum / R) < ORACLE_NEAR_EPS;",
+        "*near = fabs(u - cum / R) < ORACLE_NEAR_EPS;"),
+    "draw_upper_edge_dropped": (
+        "*near = fabs(u - prev / R) < ORACLE_NEAR_EPS || fabs(u - cum / R) < ORACLE_NEAR_EPS;",
+        "*near = fabs(u - prev / R) < ORACLE_NEAR_EPS;"),
+    "accept_band_on_products": ("if (fabs(u[t] - ratio) < ORACLE_NEAR_EPS) fl |= ORACLE_NEAR_ACCEPT;",
+                                "if (fabs(u[t] * b - a) < ORACLE_NEAR_EPS) fl |= ORACLE_NEAR_ACCEPT;"),
+    "accept_flags_every_position": ("if (!(u[t] * b < a)) { n = t; break; }",
+                                    "if (!(u[t] * b < a) && n == K) n = t;"),
+    "topp_prev_edge_dropped": (
+        "(fabs(cum / zk - p) < ORACLE_NEAR_EPS || (cut > 0 && fabs(prev / zk - p) < ORACLE_NEAR_EPS))",
+        "(fabs(cum / zk - p) < ORACLE_NEAR_EPS)"),
+    "topp_band_unnormalised": (
+        "(fabs(cum / zk - p) < ORACLE_NEAR_EPS || (cut > 0 && fabs(prev / zk - p) < ORACLE_NEAR_EPS))",
+        "(fabs(cum - p) < ORACLE_NEAR_EPS || (cut > 0 && fabs(prev - p) < ORACLE_NEAR_EPS))"),
+    "near_band_ten_times_wider": ("#define ORACLE_NEAR_EPS 1e-6", "#define ORACLE_NEAR_EPS 1e-5", "oracle.h"),
+    "near_band_ten_times_narrower": ("#define ORACLE_NEAR_EPS 1e-6", "#define ORACLE_NEAR_EPS 1e-7", "oracle.h"),
 }
 
 
 def _run_mutant(name, tmp):
-    old, new = MUTANTS[name]
-    src = open(SRC).read()
-    assert src.count(old) == 1, "mutation site for %s not found exactly once" % name
+    old, new, *where = MUTANTS[name]
+    fname = where[0] if where else "oracle.c"
     d = os.path.join(tmp, name)
     os.makedirs(d)
-    shutil.copy(os.path.join(ROOT, "oracle", "oracle.h"), d)
-    with open(os.path.join(d, "oracle.c"), "w") as f:
+    for f in ("oracle.c", "oracle.h"):
+        shutil.copy(os.path.join(ORACLE_DIR, f), d)
+    src = open(os.path.join(ORACLE_DIR, fname)).read()
+    assert src.count(old) == 1, "mutation site for %s not found exactly once" % name
+    with open(os.path.join(d, fname), "w") as f:
         f.write(src.replace(old, new))
     so = os.path.join(d, "libmutant.so")
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", so,
