@@ -232,7 +232,10 @@ spec_status spec_read_row_stats(const spec_params* params, int32_t is_verify,
  * SPEC_NOALLOC_SCRATCH_BYTES in device global memory, defined in the library,
  * which every GPU that loads the library keeps until the process exits.  The
  * first call on a device (made with that device current) looks up the array's
- * device address once; make that first call before any stream capture.
+ * device address once; make that first call before any stream capture.  The
+ * address is kept for the life of the process, so do not call this entry point
+ * again after cudaDeviceReset on that device.  params->stream must belong to
+ * the current device (else SPEC_ERR_INVALID_ARG, nothing launched).
  *
  *   - Every call uses the same array, which keeps the last call's contents.
  *     The array starts zeroed and every call leaves its counters at zero, so

@@ -166,7 +166,8 @@ def accept_histogram(num_accepted, K):
 
 def verify_threaded(target, draft, tokens, uniforms, threads, **kw):
     """Run `verify` over contiguous sequence slices on `threads` host threads (ctypes
-    releases the GIL).  Same result as `verify`; used only to time the oracle on many cores."""
+    releases the GIL).  Same result as `verify` (row_stats included when asked for);
+    used to time the oracle on many cores and to check full-size launches quickly."""
     B = tokens.shape[0]
     bounds = np.linspace(0, B, threads + 1).astype(int)
     parts = [None] * threads
@@ -183,7 +184,33 @@ def verify_threaded(target, draft, tokens, uniforms, threads, **kw):
     for t in ts:
         t.join()
     parts = [p for p in parts if p is not None]
+    res = dict(tokens=np.concatenate([p["tokens"] for p in parts]),
+               num_accepted=np.concatenate([p["num_accepted"] for p in parts]),
+               flags=np.concatenate([p["flags"] for p in parts]),
+               status=next((p["status"] for p in parts if p["status"]), 0))
+    if kw.get("with_stats"):
+        res["row_stats"] = np.concatenate([p["row_stats"] for p in parts])
+    return res
+
+
+def sample_draft_threaded(draft, uniforms, threads, **kw):
+    """`sample_draft` over contiguous sequence slices on `threads` host threads; same
+    result as `sample_draft` (the tests use it to check full-size launches quickly)."""
+    B = draft.shape[0]
+    bounds = np.linspace(0, B, threads + 1).astype(int)
+    parts = [None] * threads
+
+    def work(i):
+        a, b = bounds[i], bounds[i + 1]
+        if b > a:
+            parts[i] = sample_draft(draft[a:b], None if uniforms is None else uniforms[a:b], **kw)
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(threads)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    parts = [p for p in parts if p is not None]
     return dict(tokens=np.concatenate([p["tokens"] for p in parts]),
-                num_accepted=np.concatenate([p["num_accepted"] for p in parts]),
                 flags=np.concatenate([p["flags"] for p in parts]),
                 status=next((p["status"] for p in parts if p["status"]), 0))

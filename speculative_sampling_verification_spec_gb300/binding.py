@@ -164,43 +164,64 @@ def spec_sample_draft_workspace_size(B, K, V, dtype, greedy=False) -> int:
     return int(lib().spec_sample_draft_workspace_size(ctypes.byref(p)))
 
 
+class _VerifyArgs:
+    pass
+
+
+def _verify_args(target, draft, draft_tokens, uniforms, B=None, out_tokens=None, out_num_accepted=None,
+                 stream=None):
+    """Checks and conversions shared by every verify entry point: CUDA tensors, one
+    logit dtype (float32 or bfloat16) for both models, unit stride along V, int32
+    tokens and float64 uniforms (both made contiguous), and the output tensors.
+    Converted copies are recorded on `stream` so the allocator keeps them until the
+    call's kernels have read them."""
+    _check_cuda(target, draft, draft_tokens, uniforms)
+    a = _VerifyArgs()
+    a.K = draft_tokens.shape[1]
+    a.B = draft_tokens.shape[0] if B is None else B
+    a.V = target.shape[-1]
+    a.dt = _dtype_code(target)
+    if draft is not None and draft.dtype != target.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    if target.stride(-1) != 1 or (draft is not None and draft.stride(-1) != 1):
+        raise ValueError("logit rows must be contiguous along the vocabulary")
+    if uniforms is not None and uniforms.dtype != torch.float64:
+        raise TypeError("uniforms must be float64")
+    a.tstr = (target.stride(0), target.stride(1))
+    a.dstr = (draft.stride(0), draft.stride(1)) if draft is not None else (0, 0)
+    tok = draft_tokens if draft_tokens.dtype == torch.int32 else draft_tokens.to(torch.int32)
+    a.tok = tok.contiguous()
+    a.u = None if uniforms is None else uniforms.contiguous()
+    if stream is not None:
+        for t, orig in ((a.tok, draft_tokens), (a.u, uniforms)):
+            if t is not None and t.data_ptr() != orig.data_ptr():
+                t.record_stream(stream)
+    dev = target.device
+    a.out_tokens = torch.empty((a.B, a.K + 1), dtype=torch.int32, device=dev) if out_tokens is None else out_tokens
+    a.out_n = torch.empty((a.B,), dtype=torch.int32, device=dev) if out_num_accepted is None else out_num_accepted
+    for o, shape in ((a.out_tokens, (a.B, a.K + 1)), (a.out_n, (a.B,))):
+        if o.dtype != torch.int32 or tuple(o.shape) != shape or not o.is_contiguous() or not o.is_cuda:
+            raise ValueError("outputs must be contiguous int32 CUDA tensors of shape %s" % (shape,))
+    return a
+
+
 def spec_verify(target, draft, draft_tokens, uniforms, *, temperature=1.0, top_k=0, top_p=1.0,
                 greedy=False, out_tokens=None, out_num_accepted=None, status=None, ws=None,
                 stream=None, B=None):
     """target [B, K+1, V] and draft [B, K, V] CUDA logits (any element strides for the
     first two dims, unit stride along V), draft_tokens [B, K] int32, uniforms [B, K+1]
     float64.  Returns (out_tokens [B, K+1] int32, out_num_accepted [B] int32)."""
-    _check_cuda(target, draft, draft_tokens, uniforms)
-    K = draft_tokens.shape[1]
-    B = draft_tokens.shape[0] if B is None else B
-    V = target.shape[-1]
-    dt = _dtype_code(target)
-    if draft is not None and draft.dtype != target.dtype:
-        raise TypeError("target and draft logits must share a dtype")
-    if target.stride(-1) != 1 or (draft is not None and draft.stride(-1) != 1):
-        raise ValueError("logit rows must be contiguous along the vocabulary")
-    dev = target.device
-    if out_tokens is None:
-        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
-    if out_num_accepted is None:
-        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
-    tstr = (target.stride(0), target.stride(1))
-    dstr = (draft.stride(0), draft.stride(1)) if draft is not None else (0, 0)
-    p = make_params(B, K, V, dt, tstr, dstr, temperature, top_k, top_p, greedy,
+    a = _verify_args(target, draft, draft_tokens, uniforms, B, out_tokens, out_num_accepted, stream)
+    p = make_params(a.B, a.K, a.V, a.dt, a.tstr, a.dstr, temperature, top_k, top_p, greedy,
                     _stream_handle(stream), status)
     if ws is None:
-        ws = workspace(int(lib().spec_verify_workspace_size(ctypes.byref(p))), dev)
+        ws = workspace(int(lib().spec_verify_workspace_size(ctypes.byref(p))), target.device)
     p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
-    tok = draft_tokens if draft_tokens.dtype == torch.int32 else draft_tokens.to(torch.int32)
-    u = uniforms
-    if u is not None and u.dtype != torch.float64:
-        raise TypeError("uniforms must be float64")
-    code = lib().spec_verify(_ptr(target), _ptr(draft), _ptr(tok.contiguous()),
-                             _ptr(None if u is None else u.contiguous()), ctypes.byref(p),
-                             _ptr(out_tokens), _ptr(out_num_accepted))
+    code = lib().spec_verify(_ptr(target), _ptr(draft), _ptr(a.tok), _ptr(a.u), ctypes.byref(p),
+                             _ptr(a.out_tokens), _ptr(a.out_n))
     if code != SPEC_OK:
         raise SpecError(code, "spec_verify")
-    return out_tokens, out_num_accepted
+    return a.out_tokens, a.out_n
 
 
 def spec_sample_draft(draft, uniforms, *, temperature=1.0, top_k=0, top_p=1.0, greedy=False,
@@ -247,22 +268,14 @@ def spec_verify_noalloc(target, draft, draft_tokens, uniforms, *, temperature=1.
     """spec_verify with the library's fixed scratch array instead of a workspace, for
     callers that may not allocate device memory (see include/spec_verify.h).  Same
     arguments and results as spec_verify."""
-    _check_cuda(target, draft, draft_tokens, uniforms)
-    K, B, V = draft_tokens.shape[1], draft_tokens.shape[0], target.shape[-1]
-    dev = target.device
-    if out_tokens is None:
-        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
-    if out_num_accepted is None:
-        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
-    dstr = (draft.stride(0), draft.stride(1)) if draft is not None else (0, 0)
-    p = make_params(B, K, V, _dtype_code(target), (target.stride(0), target.stride(1)), dstr,
-                    temperature, top_k, top_p, greedy, _stream_handle(stream), status)
-    code = lib().spec_verify_noalloc(_ptr(target), _ptr(draft), _ptr(draft_tokens.contiguous()),
-                                     _ptr(None if uniforms is None else uniforms.contiguous()),
-                                     ctypes.byref(p), _ptr(out_tokens), _ptr(out_num_accepted))
+    a = _verify_args(target, draft, draft_tokens, uniforms, None, out_tokens, out_num_accepted, stream)
+    p = make_params(a.B, a.K, a.V, a.dt, a.tstr, a.dstr, temperature, top_k, top_p, greedy,
+                    _stream_handle(stream), status)
+    code = lib().spec_verify_noalloc(_ptr(target), _ptr(draft), _ptr(a.tok), _ptr(a.u), ctypes.byref(p),
+                                     _ptr(a.out_tokens), _ptr(a.out_n))
     if code != SPEC_OK:
         raise SpecError(code, "spec_verify_noalloc")
-    return out_tokens, out_num_accepted
+    return a.out_tokens, a.out_n
 
 
 def spec_accept_histogram(out_num_accepted, K, *, hist=None, stream=None):
@@ -332,36 +345,19 @@ def spec_verify_ragged(target, draft, draft_tokens, uniforms, draft_lengths, *, 
     final draw), draft_lengths: host ints K_b in [1, K] (list, numpy or CPU tensor).
     Returns (out_tokens [B, K+1], out_num_accepted [B])."""
     import numpy as np
-    _check_cuda(target, draft, draft_tokens, uniforms)
-    K = draft_tokens.shape[1]
-    B, V = draft_tokens.shape[0], target.shape[-1]
+    a = _verify_args(target, draft, draft_tokens, uniforms, None, out_tokens, out_num_accepted, stream)
     lens = np.ascontiguousarray(np.asarray(draft_lengths.cpu() if torch.is_tensor(draft_lengths) else draft_lengths,
                                            dtype=np.int32))
-    if lens.shape != (B,):
+    if lens.shape != (a.B,):
         raise ValueError("draft_lengths must hold one length per sequence")
-    dt = _dtype_code(target)
-    if draft is not None and draft.dtype != target.dtype:
-        raise TypeError("target and draft logits must share a dtype")
-    if target.stride(-1) != 1 or (draft is not None and draft.stride(-1) != 1):
-        raise ValueError("logit rows must be contiguous along the vocabulary")
-    dev = target.device
-    if out_tokens is None:
-        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
-    if out_num_accepted is None:
-        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
-    dstr = (draft.stride(0), draft.stride(1)) if draft is not None else (0, 0)
-    p = make_params(B, K, V, dt, (target.stride(0), target.stride(1)), dstr, temperature, top_k, top_p, greedy,
+    p = make_params(a.B, a.K, a.V, a.dt, a.tstr, a.dstr, temperature, top_k, top_p, greedy,
                     _stream_handle(stream), status)
     if ws is None:
-        ws = workspace(int(lib().spec_verify_ragged_workspace_size(ctypes.byref(p))), dev)
+        ws = workspace(int(lib().spec_verify_ragged_workspace_size(ctypes.byref(p))), target.device)
     p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
-    tok = draft_tokens if draft_tokens.dtype == torch.int32 else draft_tokens.to(torch.int32)
-    if uniforms is not None and uniforms.dtype != torch.float64:
-        raise TypeError("uniforms must be float64")
-    code = lib().spec_verify_ragged(_ptr(target), _ptr(draft), _ptr(tok.contiguous()),
-                                    _ptr(None if uniforms is None else uniforms.contiguous()),
-                                    lens.ctypes.data_as(ctypes.c_void_p), ctypes.byref(p), _ptr(out_tokens),
-                                    _ptr(out_num_accepted))
+    code = lib().spec_verify_ragged(_ptr(target), _ptr(draft), _ptr(a.tok), _ptr(a.u),
+                                    lens.ctypes.data_as(ctypes.c_void_p), ctypes.byref(p), _ptr(a.out_tokens),
+                                    _ptr(a.out_n))
     if code != SPEC_OK:
         raise SpecError(code, "spec_verify_ragged")
-    return out_tokens, out_num_accepted
+    return a.out_tokens, a.out_n

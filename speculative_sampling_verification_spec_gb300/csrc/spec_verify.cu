@@ -2909,10 +2909,16 @@ std::mutex g_noalloc_mu;
 void* g_noalloc_addr[64] = {};
 
 // The array's name is only a host-side stand-in: its device address is looked
-// up once per device, with that device current, and reused.
-spec_status noalloc_address(void** out) {
+// up once per device, with that device current, and reused.  The stream must
+// belong to that device, or the kernels would be given another GPU's address.
+spec_status noalloc_address(void* stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
+  if (stream) {
+    int sdev = -1;
+    if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (sdev != dev) return SPEC_ERR_INVALID_ARG;
+  }
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_addr[dev]) {
     void* ptr = nullptr;
@@ -2937,7 +2943,7 @@ extern "C" spec_status spec_verify_noalloc(const void* target_logits, const void
   if (need == 0) return SPEC_ERR_INVALID_ARG;
   if (need > kNoAllocBytes) return SPEC_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
-  const spec_status s = noalloc_address(&scratch);
+  const spec_status s = noalloc_address(p.stream, &scratch);
   if (s != SPEC_OK) return s;
   p.workspace = scratch;
   p.workspace_bytes = kNoAllocBytes;

@@ -4,6 +4,7 @@ import numpy as np
 import torch
 
 import oracle
+from _report import record
 
 NEAR_ANY = oracle.NEAR_ACCEPT | oracle.NEAR_DRAW | oracle.NEAR_TOPP
 
@@ -33,6 +34,7 @@ def compare_verify(gpu_tokens, gpu_n, ref, where=""):
         raise AssertionError("%s: %d mismatching sequences, e.g. %s: gpu n=%s tok=%s | oracle n=%s tok=%s" % (
             where, len(bad), idx.tolist(), gn[idx].tolist(), gt[idx].tolist(),
             ref["num_accepted"][idx].tolist(), ref["tokens"][idx].tolist()))
+    record(where or "verify", len(gn), int(flagged.sum()))
     return int(flagged.sum())
 
 

@@ -53,6 +53,52 @@ def test_noalloc_matches_spec_verify_twice(name, kw):
         assert torch.equal(out_t, ref_t) and torch.equal(out_n, ref_n)
 
 
+def test_noalloc_across_changing_layouts():
+    """Calls in a row that change B, K, V and the mode (greedy, top-k, unfiltered,
+    top-p on unaligned rows) share the one array: each call must still return
+    spec_verify's outputs, so no call may leave a stale counter behind."""
+    import speculative_sampling_verification_spec_gb300 as sv
+    b = sv.binding
+    L = b.lib()
+    order = [("c4", dict(B=16)), ("c5", dict(B=4)), ("c2", {}), ("c3", dict(B=6, V=50001)), ("c4", dict(B=16)),
+             ("c5", dict(B=2, V=70003))]
+    for name, kw in order:
+        w = workloads.make(name, **kw)
+        prm = params_of(w)
+        tgt, drf = to_dev(w["target"]), to_dev(w["draft"])
+        ud, uv = to_dev(w["u_draft"]), to_dev(w["u_verify"])
+        tok = sv.spec_sample_draft(drf, None if w["greedy"] else ud, **prm)
+        ref_t, ref_n = sv.spec_verify(tgt, drf, tok, uv, **prm)
+        out_t = torch.full_like(ref_t, -9)
+        out_n = torch.full_like(ref_n, -9)
+        code = _c_call(L, b, tgt, drf, tok, uv, prm, out_t, out_n)
+        assert code == 0, b.spec_status_string(code)
+        torch.cuda.synchronize()
+        assert torch.equal(out_t, ref_t) and torch.equal(out_n, ref_n), name
+
+
+def test_noalloc_python_wrapper_checks_its_inputs():
+    """The Python wrapper converts int64 draft tokens to int32 (the C entry point
+    reads int32) and rejects logits that are not contiguous along V and uniforms
+    that are not float64, as spec_verify's wrapper does."""
+    import speculative_sampling_verification_spec_gb300 as sv
+    w = workloads.make("c5", B=3, V=30000)
+    prm = params_of(w)
+    tgt, drf = to_dev(w["target"]), to_dev(w["draft"])
+    uv = to_dev(w["u_verify"])
+    tok = sv.spec_sample_draft(drf, to_dev(w["u_draft"]), **prm)
+    ref_t, ref_n = sv.spec_verify(tgt, drf, tok, uv, **prm)
+    got_t, got_n = sv.spec_verify_noalloc(tgt, drf, tok.to(torch.int64), uv, **prm)
+    torch.cuda.synchronize()
+    assert torch.equal(got_t, ref_t) and torch.equal(got_n, ref_n)
+    strided = torch.zeros(3, 9, 2 * 30000, dtype=tgt.dtype, device=tgt.device)[:, :, ::2]
+    strided.copy_(tgt)
+    with pytest.raises(ValueError):
+        sv.spec_verify_noalloc(strided, drf, tok, uv, **prm)
+    with pytest.raises(TypeError):
+        sv.spec_verify_noalloc(tgt, drf, tok, uv.float(), **prm)
+
+
 def test_noalloc_rejects_requests_beyond_its_scratch():
     import speculative_sampling_verification_spec_gb300 as sv
     b = sv.binding
