@@ -374,6 +374,7 @@ struct alignas(128) Scratch {
 // Sort keys of the row merge (in the consumed segment buffer, after the pool).
 struct SortBuf {
   unsigned long long* skey;  // [kPool]
+  uint8_t* segof;            // [kListTable]: the row merge's entry -> segment table
 };
 static_assert(sizeof(Scratch) <= 8192, "shared scratch grew past its budget");
 static_assert(kCap % kThreads == 0 && kPool % kThreads == 0, "lists are split evenly over the threads");
@@ -1704,7 +1705,7 @@ __device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int3
   if (a.filt && !sm.row_over && !(sm.row_flags & kSegBad) && total <= kListTable) {
     const float floor_v = (a.top_k > 0) ? fmaxf(sm.row_kth, kfloor) : -INFINITY;
     // entry -> segment table (one byte per entry; ns <= kThreads <= 255)
-    uint8_t* segof = reinterpret_cast<uint8_t*>(sb.skey + kPool);
+    uint8_t* segof = sb.segof;
     for (int s = tid; s < ns; s += kThreads)
       for (int i = 0, e = min(stage[s].ncand, lim); i < e; ++i) segof[stage[s].off + i] = static_cast<uint8_t>(s);
     __syncthreads();
@@ -1925,6 +1926,57 @@ struct Seg<uint16_t> {  // bf16 bits, 8 per vector
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
+  __device__ static float pw_max(uint32_t w) { return max_nan(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
+  // Bit i set when element i is >= f (ordered compare: NaN never passes), on
+  // packed pairs.  f must lie on the bf16 grid.
+  __device__ static uint32_t ge_mask(const uint4& q, float f) {
+    const uint32_t fb = __float_as_uint(f) >> 16;
+    const uint32_t tw = fb | (fb << 16);
+    __nv_bfloat162 t;
+    memcpy(&t, &tw, 4);
+    uint32_t m = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t x = word_of(q, w);
+      __nv_bfloat162 xv;
+      memcpy(&xv, &x, 4);
+      const uint32_t r = __hge2_mask(xv, t);
+      m |= ((r & 1u) | ((r >> 15) & 2u)) << (2 * w);
+    }
+    return m;
+  }
+  // the compare value of a threshold: bf16 grid values and keys' floors stay
+  // the same set under truncation; -inf becomes the lowest finite value, so
+  // that -inf elements never pass
+  __device__ static float grid_floor(float t) {
+    return __uint_as_float(__float_as_uint(fmaxf(t, -3.402823466e38f)) & 0xffff0000u);
+  }
+  // NaN-propagating max of NV vectors, on packed pairs; pw[j] keeps vector j's
+  // packed maximum (pw_max gives its value)
+  template <int NV>
+  __device__ static float lane_max(const uint4 (&q)[NV], uint32_t (&pw)[NV]) {
+    uint32_t w[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      __nv_bfloat162 a, b, c, d;
+      memcpy(&a, &q[j].x, 4);
+      memcpy(&b, &q[j].y, 4);
+      memcpy(&c, &q[j].z, 4);
+      memcpy(&d, &q[j].w, 4);
+      const __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+      memcpy(&w[j], &m, 4);
+      pw[j] = w[j];
+    }
+#pragma unroll
+    for (int j = 1; j < NV; ++j) {
+      __nv_bfloat162 a, b;
+      memcpy(&a, &w[0], 4);
+      memcpy(&b, &w[j], 4);
+      const __nv_bfloat162 m = __hmax2_nan(a, b);
+      memcpy(&w[0], &m, 4);
+    }
+    return max_nan(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xffff0000u));
+  }
   // NaN-propagating max of the vector, on packed pairs
   __device__ static float vmax(const uint4& q) {
     __nv_bfloat162 a, b, c, d;
@@ -1955,6 +2007,23 @@ struct Seg<float> {  // 4 per vector
     return max_nan(max_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
                    max_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
   }
+  __device__ static uint32_t ge_mask(const uint4& q, float f) {
+    return (__uint_as_float(q.x) >= f ? 1u : 0u) | (__uint_as_float(q.y) >= f ? 2u : 0u) |
+           (__uint_as_float(q.z) >= f ? 4u : 0u) | (__uint_as_float(q.w) >= f ? 8u : 0u);
+  }
+  __device__ static float grid_floor(float t) { return fmaxf(t, -3.402823466e38f); }
+  template <int NV>
+  __device__ static float lane_max(const uint4 (&q)[NV], uint32_t (&pw)[NV]) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const float v = vmax(q[j]);
+      pw[j] = __float_as_uint(v);
+      m = max_nan(m, v);
+    }
+    return m;
+  }
+  __device__ static float pw_max(uint32_t w) { return __uint_as_float(w); }
 };
 
 // Bitonic sort of one value per lane, descending across the warp.
@@ -2364,7 +2433,8 @@ __global__ void __launch_bounds__(kThreads, sizeof(E) == 4 ? 8 : 5) spec_row_ker
   unsigned char* scratch = smem_raw + sizeof(Scratch);
   int32_t* pool_idx = reinterpret_cast<int32_t*>(scratch);
   float* pool_val = reinterpret_cast<float*>(pool_idx + kPool);
-  const SortBuf sb{reinterpret_cast<unsigned long long*>(pool_val + kPool)};
+  const SortBuf sb{reinterpret_cast<unsigned long long*>(pool_val + kPool),
+                   reinterpret_cast<uint8_t*>(pool_val + kPool + 2 * kPool)};
   // launched as a programmatic dependent of the segment kernel: wait until that
   // grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -2391,6 +2461,627 @@ __global__ void __launch_bounds__(kThreads, sizeof(E) == 4 ? 8 : 5) spec_row_ker
     }
     __syncthreads();
   }
+}
+
+
+// ---------------------------------------------------------------------------
+// The one-launch streaming kernel (rows whose starts are 16-byte aligned;
+// greedy, or top-k with k <= kSK).
+//
+// A persistent grid, four CTAs per SM; CTA c takes rows c, c + G, c + 2G, ...
+// in order, so whole sequences complete one after another through the launch
+// and the work after a row (its cut and record, and a sequence's accept tests
+// and final draw) overlaps the streaming of other rows.  A row never leaves
+// its CTA: there is no cross-CTA merge.
+//
+//   * Each warp owns a ring of kSNS 3-KB buffers that bulk copies fill; a row
+//     is walked in warp-stages of kSWV vectors, warp w taking stages w, w + 4,
+//     ...  Lane 0 keeps the ring full, running ahead through this warp's
+//     stages of its next rows, so a warp waits only for its own copies and
+//     never for a row boundary.
+//   * Per stage and lane: the max of its six vectors (packed bf16 pairs for
+//     bf16) against the running max; only a new max looks at single elements
+//     (its first index).
+//   * Top-k: a warp keeps every element at or above its threshold in its own
+//     candidate buffer.  The threshold starts at the k-th largest vector
+//     maximum of the warp's first stage (at least k elements lie at or above
+//     it) and rises to the k-th largest buffered value whenever the buffer
+//     passes a high-water mark.  Each such value bounds the row's k-th value
+//     from below, so a warp also takes any higher value another warp
+//     publishes.  A lane whose six vectors all lie below the threshold does no
+//     more work for the stage.
+//   * Row end: the buffered values at or above the largest per-warp k-th
+//     value are ranked in shared memory (value desc, index asc); the first k,
+//     then the top-p prefix within them, are the kept set, written in index
+//     order with the row record.  Ties or a buffer too small for a stage send
+//     the row to the exact general path.  The CTA that completes a sequence (a
+//     counter) runs its accept tests and final draw.
+
+constexpr int kSK = 64;            // largest top-k the streaming kernel collects
+constexpr int kSWV = 192;          // vectors per warp-stage (3 KB)
+constexpr int kSVPL = kSWV / 32;   // vectors per lane and stage
+constexpr int kSNS = 3;            // buffers per warp
+constexpr int kSWCap = 256;        // candidate entries per warp
+constexpr int kSKeys = 512;        // row-end ranking capacity (keys in the Scratch's candidate arrays)
+constexpr size_t kSStage = static_cast<size_t>(kSWV) * 16;
+constexpr size_t kSRing = static_cast<size_t>(kWarps) * kSNS * kSStage;
+constexpr size_t kSCand = static_cast<size_t>(kWarps) * kSWCap * sizeof(uint2);
+static_assert(kCap * sizeof(unsigned long long) <= kSCand, "the general path's sort keys fit the candidate buffers");
+static_assert(kListTable <= sizeof(int32_t) * kCap + sizeof(float) * kCap &&
+                  kSKeys * sizeof(unsigned long long) <= sizeof(int32_t) * kCap + sizeof(float) * kCap,
+              "the merge's entry table and the row-end keys fit the Scratch's candidate arrays");
+static_assert(kSK <= kSWV && 4 * kSK <= kSWCap && kSK <= 64, "a warp's first stage and buffer hold k candidates");
+
+struct alignas(128) StreamHdr {
+  uint64_t bar[kWarps * kSNS];  // completion of each warp's buffers
+  float wthr[kWarps];           // published warp thresholds of the current row
+  float wkth[kWarps];           // row end: each warp's k-th buffered value
+  float wmax[kWarps];
+  int32_t warg[kWarps];
+  int32_t wflag[kWarps];        // row end: kSegOver
+  int32_t wfill[kWarps];        // entries in each warp's buffer (slots taken by atomics)
+  int32_t nlist;                // row end: keys gathered
+  float f2;                     // row end: the row's k-th largest group max
+  int32_t cut;                  // row end: rank of the last kept entry
+  FF zf;                        // row end: kept mass
+  int32_t last;                 // this CTA completed the sequence
+};
+
+template <int PASS_CAND>
+__host__ __device__ constexpr size_t stream_smem_bytes() {
+  return sizeof(Scratch) + sizeof(StreamHdr) + kSRing + (PASS_CAND ? kSCand : 0);
+}
+
+// Largest t whose set bits lie in the top KB bits such that at least `need`
+// of the warp's keys key(0..PER-1) are >= t; 0 when fewer than `need` keys are
+// nonzero (a zero key counts for nothing).  Same value on every lane.
+template <int PER, int KB, typename KeyOf>
+__device__ __forceinline__ uint32_t warp_select_key(KeyOf key_of, int need) {
+  uint32_t t = 0;
+#pragma unroll 1
+  for (int bit = 31; bit >= 32 - KB; --bit) {
+    const uint32_t c = t | (1u << bit);
+    int n = 0;
+#pragma unroll
+    for (int p = 0; p < PER; ++p) n += (key_of(p) >= c) ? 1 : 0;
+    if (static_cast<int>(__reduce_add_sync(FULL, static_cast<unsigned>(n))) >= need) t = c;
+  }
+  return t;
+}
+
+// The float a key threshold t compares as: for data on the element grid,
+// x >= key_floor(t) iff okey32(x) >= t (bf16 keys compare on their top 16 bits).
+__device__ __forceinline__ float key_floor(uint32_t t) { return t ? okey32_val(t) : -INFINITY; }
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+
+// The k-th largest value of a warp's buffer of n entries (-inf when fewer).
+template <typename E>
+__device__ __forceinline__ float warp_buffer_kth(const uint2* wc, int n, int k) {
+  constexpr int KB = sizeof(E) == 2 ? 16 : 32;
+  constexpr int PER = kSWCap / 32;
+  const int lane = threadIdx.x & 31;
+  uint32_t key[PER];
+#pragma unroll
+  for (int p = 0; p < PER; ++p) {
+    const int i = p * 32 + lane;
+    key[p] = (i < n) ? okey32(__uint_as_float(wc[i].y)) : 0u;
+  }
+  return key_floor(warp_select_key<PER, KB>([&](int p) { return key[p]; }, k));
+}
+
+// Drop the buffer entries below f (order kept); returns the new count.
+__device__ __forceinline__ int warp_buffer_compact(uint2* wc, int n, float f) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  int out = 0;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    uint2 e = make_uint2(0u, 0u);
+    bool keep = false;
+    if (i < n) {
+      e = wc[i];
+      keep = __uint_as_float(e.y) >= f;
+    }
+    const unsigned km = __ballot_sync(FULL, keep);  // every lane has read its entry
+    if (keep) wc[out + __popc(km & lt)] = e;
+    out += __popc(km);
+  }
+  __syncwarp();
+  return out;
+}
+
+// This warp's part of a row: its stages, the row's whole vectors and their
+// address (issue cursor of the ring).
+struct RowRing {
+  int my, nw;
+  const uint4* src;
+};
+template <typename E, bool RAG>
+__device__ __noinline__ RowRing row_ring(const KArgs& a, int row, int warp) {
+  constexpr int N = Seg<E>::N;
+  const RowInfo ri = decode_job<RAG>(a, row);
+  RowRing r;
+  const int nv = (a.V + N - 1) / N, nst = (nv + kSWV - 1) / kSWV;
+  r.my = (nst > warp) ? (nst - warp + kWarps - 1) / kWarps : 0;
+  r.nw = a.V / N;
+  r.src = reinterpret_cast<const uint4*>(static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off);
+  return r;
+}
+
+// The row record, the draw of a sampled row, and (rows before a sequence's
+// last draft position) the draft token's adjusted probability.  One thread.
+// kept: the cut (tv, ti) and mass zf; list_len < 0 when no list is stored.
+// wd(d): the weight of token d when it is kept, else 0.
+template <typename WD>
+__device__ void stream_record(const KArgs& a, const RowInfo& ri, float m, int argmax, bool bad, Cut cut, FF zf,
+                              int list_len, int tok, WD wd) {
+  spec_row_stat* rec = a.rows + ri.job;
+  int flags = bad ? kFlagNonfinite : 0;
+  double p_tok = 0.0;
+  if (a.mode == kModeVerify && ri.t < ri.kb && !a.fused) {
+    const int d = a.tokens[static_cast<int64_t>(ri.b) * a.K + ri.t];
+    if (d < 0 || d >= a.V) {
+      flags |= kFlagToken;
+    } else if (!bad && !a.greedy) {
+      const float w = wd(d);
+      if (w > 0.0f) p_tok = static_cast<double>(w) / ff_to_d(zf);
+    }
+  }
+  if (a.mode == kModeSample || (a.fused && !ri.is_target)) {
+    if (a.fused) a.out_draft[ri.b] = tok;
+    else a.out_tokens[static_cast<int64_t>(ri.b) * a.K + ri.t] = tok;
+    rec->token = tok;
+    if (a.mode == kModeSample && bad) set_status(a, SPEC_ERR_NONFINITE);
+  }
+  rec->zf = ff_to_d(zf);
+  rec->p_tok = p_tok;
+  rec->m = m;
+  rec->tau_val = cut.tv;
+  rec->tau_idx = cut.ti;
+  rec->argmax = argmax;
+  rec->list_len = list_len;
+  rec->flags = flags;
+}
+
+// RAG: a ragged call; CAND: top-k candidates (else greedy: max and argmax).
+template <typename E, bool RAG, bool CAND>
+__global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
+  StreamHdr& hd = *reinterpret_cast<StreamHdr*>(smem_raw + sizeof(Scratch));
+  unsigned char* ring = smem_raw + sizeof(Scratch) + sizeof(StreamHdr);
+  unsigned char* cand = ring + kSRing;  // CAND: the warps' buffers
+  constexpr int N = Seg<E>::N;
+  constexpr int KB = sizeof(E) == 2 ? 16 : 32;  // significant key bits of an element
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned char* wring = ring + static_cast<size_t>(warp) * kSNS * kSStage;
+  uint64_t* wbar = hd.bar + warp * kSNS;
+  uint2* wc = reinterpret_cast<uint2*>(cand) + warp * kSWCap;  // CAND: this warp's buffer
+  const int G = static_cast<int>(gridDim.x);
+  const int ktop = a.top_k;
+  const int hwm = max(kSWCap * 5 / 8, 2 * ktop);  // buffer entries that trigger a cut to the top k
+  const int nv = (a.V + N - 1) / N, nw = a.V / N;  // vectors of a row, whole ones
+
+  if (lane == 0) {
+    for (int b = 0; b < kSNS; ++b) mbar_init(&wbar[b], 1);
+    fence_mbar_init();
+  }
+  if (tid < kWarps) hd.wthr[tid] = -INFINITY;
+  __syncthreads();
+  uint32_t phase = 0;   // bit b: parity of buffer b's next completion
+  uint32_t pending = 0; // lane 0, bit b: buffer b has a copy whose completion was not seen
+  bool staged = true;   // this warp still uses bulk copies
+  int bnext = 0;        // buffer of this warp's next stage
+
+  // lane 0's issue cursor: row ir, its stage ik, buffer ib
+  int ir = static_cast<int>(blockIdx.x), ik = 0, ib = 0, inflight = 0;
+  RowRing ig{0, 0, nullptr};
+  if (lane == 0 && ir < a.nrows) ig = row_ring<E, RAG>(a, ir, warp);
+  auto top_up = [&]() {
+    while (staged && inflight < kSNS && ir < a.nrows) {
+      if (ik >= ig.my) {
+        ir += G;
+        ik = 0;
+        if (ir < a.nrows) ig = row_ring<E, RAG>(a, ir, warp);
+        continue;
+      }
+      const int vs = (warp + kWarps * ik) * kSWV;
+      const int nb = max(0, min(ig.nw - vs, kSWV));
+      mbar_expect_tx(&wbar[ib], static_cast<uint32_t>(nb) * 16u);
+      if (nb > 0) bulk_copy_g2s(wring + ib * kSStage, ig.src + vs, static_cast<uint32_t>(nb) * 16u, &wbar[ib]);
+      pending |= 1u << ib;
+      ib = (ib + 1 == kSNS) ? 0 : ib + 1;
+      ++ik;
+      ++inflight;
+    }
+  };
+  if (lane == 0) top_up();
+
+  for (int row = static_cast<int>(blockIdx.x); row < a.nrows; row += G) {
+    const RowInfo ri = decode_job<RAG>(a, row);
+    const E* grow = static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off;
+    const uint4* gv = reinterpret_cast<const uint4*>(grow);
+    const int nst = (nv + kSWV - 1) / kSWV;
+    const int my = (nst > warp) ? (nst - warp + kWarps - 1) / kWarps : 0;
+
+    float rmax = -INFINITY;
+    int rarg = INT_MAX;
+    float thr = -INFINITY;  // CAND: this warp's threshold (warp-uniform)
+    int wn = 0;             // CAND: entries in the warp's buffer
+    bool wover = false;     // CAND: the buffer could not take a stage
+
+    for (int k = 0; k < my; ++k) {
+      const int b = bnext;
+      bnext = (b + 1 == kSNS) ? 0 : b + 1;
+      const int vs = (warp + kWarps * k) * kSWV;
+      bool from_smem = false;
+      if (staged) {
+        bool ok = mbar_try_wait(&wbar[b], (phase >> b) & 1u);
+        if (!ok) ok = mbar_wait_bounded(&wbar[b], (phase >> b) & 1u);
+        from_smem = __all_sync(FULL, ok);
+        if (from_smem) {
+          phase ^= 1u << b;
+          pending &= ~(1u << b);
+        } else {  // a copy was lost: this warp reads the rows itself from now on
+          staged = false;
+          set_status(a, SPEC_ERR_TIMEOUT);
+        }
+      }
+      const uint32_t wbase = smem_addr(wring + b * kSStage);
+      // vector j of this lane (vector vs + 32 j + lane of the row)
+      auto vec = [&](int j) -> uint4 {
+        const int t = j * 32 + lane, v = vs + t;
+        if (v < nw) return from_smem ? ld_shared_v4(wbase + static_cast<uint32_t>(t) * 16u) : ld_stream(gv + v);
+        if (v < nv) return Seg<E>::load_some(grow, v, a.V - v * N);
+        return Seg<E>::neg_inf();
+      };
+      uint4 q[kSVPL];
+      if (from_smem && vs + kSWV <= nw) {
+#pragma unroll
+        for (int j = 0; j < kSVPL; ++j) q[j] = ld_shared_v4(wbase + static_cast<uint32_t>(j * 32 + lane) * 16u);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kSVPL; ++j) q[j] = vec(j);
+      }
+      // the lane's max over its vectors (NaN-propagating), and each vector's
+      uint32_t pw[kSVPL];
+      const float tm = Seg<E>::template lane_max<kSVPL>(q, pw);
+      // a new running max: the first element that holds it (the lane meets its
+      // elements in index order)
+      if (tm > rmax) {
+        int jf = kSVPL - 1;
+#pragma unroll
+        for (int j = kSVPL - 1; j >= 0; --j) jf = (Seg<E>::pw_max(pw[j]) == tm) ? j : jf;
+        uint4 x = q[0];
+#pragma unroll
+        for (int j = 1; j < kSVPL; ++j) x = (j == jf) ? q[j] : x;
+        int ef = 0;
+#pragma unroll
+        for (int i = N - 1; i >= 0; --i) ef = (Seg<E>::get(x, i) == tm) ? i : ef;
+        rarg = (vs + jf * 32 + lane) * N + ef;
+      }
+      rmax = max_nan(rmax, tm);
+
+      if constexpr (CAND) {
+        if (!wover) {
+          // a lane's group: its kSVPL vectors of the stage.  The row's top k
+          // elements lie in the k groups with the largest maxima, so the warp
+          // keeps (group max, group) for every group whose max reaches its
+          // threshold; the elements are picked out at the row end.
+          // The first stage: the k-th largest finite vector maximum (at least
+          // k elements reach it).
+          if (k == 0) {
+            const uint32_t t = warp_select_key<kSVPL, KB>(
+                [&](int j) {
+                  const float v = Seg<E>::pw_max(pw[j]);
+                  return (v > -INFINITY && v < INFINITY) ? okey32(v) : 0u;
+                },
+                ktop);
+            thr = fmaxf(thr, key_floor(t));
+          }
+          float te = thr;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) te = fmaxf(te, reinterpret_cast<volatile float*>(hd.wthr)[w]);
+          // a buffer past its high-water mark is cut to its k largest groups
+          // first (k group maxima at or above a value: k elements at or above it)
+          if (wn >= hwm) {
+            te = fmaxf(te, warp_buffer_kth<E>(wc, wn, ktop));
+            wn = warp_buffer_compact(wc, wn, te);
+          }
+          const bool hot = tm >= te;  // false for NaN
+          const unsigned hb = __ballot_sync(FULL, hot);
+          if (hb) {
+            const int c = __popc(hb);
+            if (wn + c > kSWCap) {
+              wover = true;  // ties beyond the buffer: the row takes the general path
+            } else {
+              if (hot) wc[wn + __popc(hb & ((1u << lane) - 1u))] = make_uint2(static_cast<uint32_t>(vs + lane), __float_as_uint(tm));
+              wn += c;
+              __syncwarp();
+            }
+          }
+          if (te > thr) {
+            thr = te;
+            if (lane == 0) hd.wthr[warp] = thr;
+          }
+        }
+      }
+      // the warp is done with the buffer: lane 0 refills the ring
+      __syncwarp();
+      if (lane == 0) {
+        --inflight;
+        top_up();
+      }
+    }
+
+    // ---- row end: max, first argmax (lowest index among the lanes that hold it)
+    float wm = rmax;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wm = max_nan(wm, __shfl_xor_sync(FULL, wm, o));
+    int wa = (rmax == wm) ? rarg : INT_MAX;  // false for NaN
+    wa = static_cast<int>(__reduce_min_sync(FULL, static_cast<unsigned>(wa)));
+    float wk = -INFINITY;
+    if constexpr (CAND) {
+      // this warp's k-th buffered value bounds the row's k-th value from below
+      if (!wover && wn >= ktop) wk = warp_buffer_kth<E>(wc, wn, ktop);
+    }
+    if (lane == 0) {
+      hd.wmax[warp] = wm;
+      hd.warg[warp] = wa;
+      hd.wkth[warp] = wk;
+      hd.wflag[warp] = wover ? kSegOver : 0;
+    }
+    if (tid == 0) hd.nlist = 0;
+    __syncthreads();
+    float m = -INFINITY, f = -INFINITY;
+    int am = INT_MAX, fl = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) m = max_nan(m, hd.wmax[w]);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      if (hd.wmax[w] == m) am = min(am, hd.warg[w]);
+      fl |= hd.wflag[w];
+      f = fmaxf(f, fmaxf(hd.wthr[w], hd.wkth[w]));
+    }
+    const bool bad = !(m == m) || m == INFINITY || !(m > -INFINITY);
+    const int argmax = (am == INT_MAX) ? -1 : am;
+    __syncthreads();  // the thresholds are read: the next row starts from none
+    if (tid < kWarps) hd.wthr[tid] = -INFINITY;
+
+    if constexpr (!CAND) {
+      if (tid == 0)
+        stream_record(a, ri, m, argmax, bad, cut_all(), ff(0.0f), -1, bad ? -1 : argmax, [](int) { return 0.0f; });
+    } else {
+      // ---- top-k: the groups whose max is >= f hold every element >= f; their
+      // elements >= f are read back from the row (the copies are gone) and
+      // ranked (value desc, index asc)
+      unsigned long long* keys = reinterpret_cast<unsigned long long*>(sm.cand_idx);
+      bool general = bad || (fl & kSegOver);
+      if (!general) {
+        // this warp's groups >= f, packed to the front of its buffer
+        wn = warp_buffer_compact(wc, wn, f);
+        if (lane == 0) hd.wflag[warp] = wn;
+      }
+      __syncthreads();
+      int g0[kWarps + 1];
+      g0[0] = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) g0[w + 1] = g0[w] + (general ? 0 : hd.wflag[w]);
+      const int ng = g0[kWarps];
+      const uint2* allc = reinterpret_cast<const uint2*>(cand);
+      auto group_at = [&](int g) {
+        int w = 0;
+#pragma unroll
+        for (int x = 1; x < kWarps; ++x) w = (g >= g0[x]) ? x : w;
+        return allc[w * kSWCap + (g - g0[w])];
+      };
+      // a tighter floor: the k-th largest group max over the whole row (at
+      // least k groups, so k elements, reach it)
+      if (!general && warp == 0) {
+        float f2 = f;
+        if (ng <= kSWCap) {
+          constexpr int PER = kSWCap / 32;
+          uint32_t key[PER];
+#pragma unroll
+          for (int p = 0; p < PER; ++p) {
+            const int g = p * 32 + lane;
+            key[p] = (g < ng) ? okey32(__uint_as_float(group_at(g).y)) : 0u;
+          }
+          f2 = fmaxf(f2, key_floor(warp_select_key<PER, KB>([&](int p) { return key[p]; }, ktop)));
+        }
+        if (lane == 0) hd.f2 = f2;
+      }
+      __syncthreads();
+      if (!general) {
+        f = hd.f2;
+        const float tf = Seg<E>::grid_floor(f);
+        // item = (group, vector of the group); the loads of a round go out together
+        constexpr int R = 4;
+        for (int base = 0; base < ng * kSVPL; base += R * kThreads) {
+          uint4 x[R];
+          int vv[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const int it = base + r * kThreads + tid;
+            vv[r] = -1;
+            x[r] = Seg<E>::neg_inf();
+            if (it < ng * kSVPL) {
+              const int g = it / kSVPL, j = it - g * kSVPL;
+              const uint2 ge = group_at(g);
+              if (__uint_as_float(ge.y) >= f) {
+                const int v = static_cast<int>(ge.x) + j * 32;
+                vv[r] = v;
+                if (v < nw) x[r] = ld_stream(gv + v);
+                else if (v < nv) x[r] = Seg<E>::load_some(grow, v, a.V - v * N);
+              }
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            if (vv[r] < 0) continue;
+            for (uint32_t mk = Seg<E>::ge_mask(x[r], tf); mk; mk &= mk - 1) {
+              const int i = __ffs(mk) - 1;
+              const int pos = atomicAdd(&hd.nlist, 1);
+              if (pos < kSKeys) keys[pos] = sort_key(Seg<E>::get(x[r], i), vv[r] * N + i);
+            }
+          }
+        }
+      }
+      __syncthreads();
+      const int n = hd.nlist;
+      general = general || n > kSKeys || n < 1;
+      unsigned long long* sorted = reinterpret_cast<unsigned long long*>(cand);  // the buffers are read
+      const int kk = min(ktop, n);
+      if (!general) {
+        const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(keys);
+        for (int i = tid; i < n; i += kThreads) {
+          const unsigned long long key = keys[i];
+          int r = 0;
+          int j = 0;
+#pragma unroll 4
+          for (; j + 1 < n; j += 2) {
+            const ulonglong2 p = k2[j >> 1];
+            r += ((p.x > key) ? 1 : 0) + ((p.y > key) ? 1 : 0);
+          }
+          if (j < n) r += (keys[j] > key) ? 1 : 0;
+          if (r < kk) sorted[r] = key;
+        }
+      }
+      __syncthreads();
+      if (!general && warp == 0) {
+        // prefix of the weights in rank order (two entries a lane), the top-p
+        // cut within the top k, and the kept mass
+        float w2[2];
+        FF pre[2];
+        FF run = ff(0.0f);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const int i = 2 * lane + g;
+          w2[g] = (i < kk) ? wexp(skey_val(sorted[i]), m, a.c) : 0.0f;
+          run = ff_add(run, w2[g]);
+          pre[g] = run;
+        }
+        const FF incl = warp_incl_scan_ff(run, lane);
+        const FF excl = ff_sub(incl, run);
+        const FF total = FF{__shfl_sync(FULL, incl.hi, 31), __shfl_sync(FULL, incl.lo, 31)};
+        int cut = kk - 1;
+        if (a.top_p < 1.0f) {
+          const FF need = ff_mul(total, a.top_p);
+          int first = INT_MAX;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int i = 2 * lane + g;
+            if (i < kk && !ff_lt(ff_add(excl, pre[g]), need)) first = min(first, i);
+          }
+          first = static_cast<int>(__reduce_min_sync(FULL, static_cast<unsigned>(first)));
+          if (first != INT_MAX) cut = first;
+        }
+        // the prefix at the cut, from the lane that holds it
+        const int hl = cut >> 1;
+        const FF zc = ff_add(excl, pre[cut & 1]);
+        const float zh = __shfl_sync(FULL, zc.hi, hl), zl = __shfl_sync(FULL, zc.lo, hl);
+        if (lane == 0) {
+          hd.cut = cut;
+          hd.zf = FF{zh, zl};
+        }
+      }
+      __syncthreads();
+      if (!general) {
+        // the kept set in index order: an entry's position is the number of
+        // kept entries with a smaller index
+        const int nkeep = hd.cut + 1;
+        const FF zf = hd.zf;
+        int32_t* lidx = a.list_idx + static_cast<int64_t>(row) * kCap;
+        float* lw = a.list_w + static_cast<int64_t>(row) * kCap;
+        int32_t* sidx = sm.cand_idx;  // the keys are read: the list, for the draw
+        float* sw = sm.cand_val;
+        int xi = -1;
+        float xw = 0.0f;
+        int xpos = 0;
+        if (tid < nkeep) {
+          xi = skey_idx(sorted[tid]);
+          xw = wexp(skey_val(sorted[tid]), m, a.c);
+          for (int j = 0; j < nkeep; ++j) xpos += (skey_idx(sorted[j]) < xi) ? 1 : 0;
+          lidx[xpos] = xi;
+          lw[xpos] = xw;
+        }
+        __syncthreads();  // every key is read
+        if (tid < nkeep) {
+          sidx[xpos] = xi;
+          sw[xpos] = xw;
+        }
+        __syncthreads();
+        const unsigned long long ck = sorted[nkeep - 1];
+        const Cut cut{skey_val(ck), skey_idx(ck)};
+        int tok = -1;
+        if (a.mode == kModeSample || (a.fused && !ri.is_target)) {
+          const double u = a.fused ? a.u_draft[ri.b] : a.u[static_cast<int64_t>(ri.b) * a.K + ri.t];
+          const int pos = list_ordered_draw(nkeep, u, sm, [&](int i) { return sw[i]; });
+          tok = (pos >= 0) ? sidx[pos] : -1;
+        }
+        // the kept weight of a token: a search of the kept list (index order)
+        auto wd = [&](int d) {
+          int lo = 0, hi = nkeep;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sidx[mid] < d) lo = mid + 1;
+            else hi = mid;
+          }
+          return (lo < nkeep && sidx[lo] == d) ? sw[lo] : 0.0f;
+        };
+        if (tid == 0) stream_record(a, ri, m, argmax, false, cut, zf, nkeep, tok, wd);
+      } else {
+        // the exact general path: the row's record says what the stream could
+        // not settle (a non-finite row, or a buffer too small for its ties)
+        if (tid == 0) {
+          SegRec* rec = a.segs + row;
+          rec->m = m;
+          rec->argmax = argmax;
+          rec->z_hi = 0.0f;
+          rec->z_lo = 0.0f;
+          rec->theta = -INFINITY;
+          rec->kth = -INFINITY;
+          rec->ncand = 0;
+          rec->flags = (bad ? kSegBad : 0) | kSegOver;
+        }
+        __syncthreads();
+        // with the record flagged, the merge gathers no pool (the pool arrays
+        // are never touched) and the general path sorts at most kCap keys in
+        // the candidate buffers
+        Local C;
+        const SortBuf sb{reinterpret_cast<unsigned long long*>(cand), reinterpret_cast<uint8_t*>(sm.cand_idx)};
+        row_finish<E>(a, ri, grow, sm, C, sb, reinterpret_cast<int32_t*>(cand), reinterpret_cast<float*>(cand));
+      }
+    }
+
+    // ---- the CTA that completes the sequence runs its epilogue
+    __syncthreads();  // every global write of the row is ordered before the sequence counter
+    if (a.mode == kModeVerify) {
+      if (tid == 0) {
+        fence_acq_rel_gpu();
+        unsigned long long* tk = &a.tickets[ri.b];
+        const bool last = atomicAdd(tk, 1ull) == static_cast<unsigned long long>(ri.nr - 1);
+        if (last) {
+          *tk = 0ull;  // the sequence's last row: no other arrival of this call
+          fence_acq_rel_gpu();
+        }
+        hd.last = last ? 1 : 0;
+      }
+      __syncthreads();
+      if (hd.last) verify_epilogue<E>(a, ri.b, ri.kb, ri.first, sm);
+    }
+    __syncthreads();  // the Scratch and the candidate buffers are free again
+  }
+  // copies whose completion was never seen (only after a lost one) must land
+  // before the shared memory is released
+  if (lane == 0)
+    for (int b = 0; b < kSNS; ++b)
+      if (pending & (1u << b)) (void)mbar_wait_bounded(&wbar[b], (phase >> b) & 1u);
 }
 
 }  // namespace
@@ -2427,6 +3118,8 @@ struct DevInfo {
   int max_smem = 0;
   size_t smem_set[8] = {};  // dynamic smem attribute set: [kernel * 4 + ragged * 2 + dtype]
   int per_sm[4] = {};       // resident segment-kernel CTAs per SM: [ragged * 2 + dtype]
+  size_t ssmem_set[8] = {}; // streaming kernel: [cand * 4 + ragged * 2 + dtype]
+  int sper_sm[8] = {};      // resident streaming-kernel CTAs per SM, same index
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
@@ -2451,6 +3144,9 @@ struct Plan {
   int esize = 0, R = 0, S = 0, nseg = 0, n0 = 0, grid = 0, row_grid = 0, seg_bytes = 0;
   bool clear_counters = false;  // more counters than the area that calls keep zeroed
   bool ragged = false;          // per-sequence draft lengths (the kernels' RAG instantiation)
+  bool aligned = false;         // every row start is 16-byte aligned
+  bool stream = false;          // the one-launch streaming kernel (else segment + row kernels)
+  int nseg_ws = 0;              // segment records per row the workspace holds
   size_t counter_bytes = 0;
   int64_t nrows = 0, items = 0;
   size_t smem = 0, row_smem = 0;  // dynamic shared memory of the segment and row kernels
@@ -2500,6 +3196,7 @@ spec_status make_plan(const spec_params* p, bool verify, Plan* pl) {
   pl->seg_bytes = static_cast<int>(round_up(static_cast<size_t>(S) * pl->esize, 128));
   pl->smem = sizeof(Scratch) + 2 * static_cast<size_t>(pl->seg_bytes);
   pl->row_smem = sizeof(Scratch) + kPool * (sizeof(int32_t) + sizeof(float) + sizeof(unsigned long long)) + kListTable;
+  pl->nseg_ws = pl->nseg;
   const size_t nr = static_cast<size_t>(pl->nrows);
   const size_t ni = static_cast<size_t>(pl->items);
   // the counter area: at offset 0 and at least kCounterArea bytes, so that a
@@ -2538,9 +3235,59 @@ spec_status set_smem(DevInfo& di, int slot, const void* fn, size_t bytes) {
   return SPEC_OK;
 }
 
+template <typename E>
+const void* stream_fn(bool rag, bool cand) {
+  if (cand)
+    return rag ? reinterpret_cast<const void*>(&spec_stream_kernel<E, true, true>)
+               : reinterpret_cast<const void*>(&spec_stream_kernel<E, false, true>);
+  return rag ? reinterpret_cast<const void*>(&spec_stream_kernel<E, true, false>)
+             : reinterpret_cast<const void*>(&spec_stream_kernel<E, false, false>);
+}
+
+// The streaming kernel takes aligned calls that are greedy, or top-k with
+// k <= kSK: a persistent grid, as many CTAs as fit at once, one row at a time
+// each (the row record and the kept list go where the two-kernel path puts
+// them; its per-row part record is written only for the general path).
+spec_status plan_stream(const spec_params* p, DevInfo& di, Plan* pl) {
+  const bool use_k = !p->greedy && p->top_k > 0 && p->top_k < p->V;
+  if (!pl->aligned || !(p->greedy || (use_k && p->top_k <= kSK))) return SPEC_OK;
+  const bool cand = !p->greedy;
+  const size_t smem = cand ? stream_smem_bytes<1>() : stream_smem_bytes<0>();
+  if (smem > static_cast<size_t>(di.max_smem)) return SPEC_OK;
+  const int which = (p->dtype == SPEC_F32) ? 0 : 1;
+  const int slot = (cand ? 4 : 0) + (pl->ragged ? 2 : 0) + which;
+  const void* fn = which == 0 ? stream_fn<float>(pl->ragged, cand) : stream_fn<uint16_t>(pl->ragged, cand);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (di.ssmem_set[slot] < smem) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+      di.ssmem_set[slot] = smem;
+    }
+    if (di.sper_sm[slot] == 0) {
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess || per_sm < 1)
+        return SPEC_ERR_CUDA;
+      di.sper_sm[slot] = per_sm;
+    }
+  }
+  const int64_t slots = static_cast<int64_t>(di.sper_sm[slot]) * di.sms;
+  pl->stream = true;
+  pl->S = p->V;
+  pl->nseg = 1;
+  pl->items = pl->nrows;
+  pl->smem = smem;
+  pl->grid = static_cast<int>(std::min<int64_t>(pl->nrows, slots));
+  return SPEC_OK;
+}
+
 // Segment kernel: a persistent grid, as many CTAs as fit at once (never more
 // than the items).  Row kernel: one CTA per row.
 spec_status plan_launch(const spec_params* p, DevInfo& di, Plan* pl) {
+  spec_status st = plan_stream(p, di, pl);
+  if (st != SPEC_OK || pl->stream) return st;
   if (pl->smem > static_cast<size_t>(di.max_smem) || pl->row_smem > static_cast<size_t>(di.max_smem))
     return SPEC_ERR_UNSUPPORTED;
   const int which = (p->dtype == SPEC_F32) ? 0 : 1;
@@ -2574,6 +3321,29 @@ spec_status launch(const spec_params* p, const Plan& pl, KArgs& a, DevInfo* di) 
   cudaStream_t st = static_cast<cudaStream_t>(p->stream);
   if (pl.clear_counters && cudaMemsetAsync(p->workspace, 0, pl.counter_bytes, st) != cudaSuccess)
     return SPEC_ERR_CUDA;
+  if (pl.stream) {
+    const bool cand = !p->greedy;
+    if (p->dtype == SPEC_F32) {
+      if (cand) {
+        if (pl.ragged) spec_stream_kernel<float, true, true><<<grid, block, pl.smem, st>>>(a);
+        else spec_stream_kernel<float, false, true><<<grid, block, pl.smem, st>>>(a);
+      } else {
+        if (pl.ragged) spec_stream_kernel<float, true, false><<<grid, block, pl.smem, st>>>(a);
+        else spec_stream_kernel<float, false, false><<<grid, block, pl.smem, st>>>(a);
+      }
+    } else {
+      if (cand) {
+        if (pl.ragged) spec_stream_kernel<uint16_t, true, true><<<grid, block, pl.smem, st>>>(a);
+        else spec_stream_kernel<uint16_t, false, true><<<grid, block, pl.smem, st>>>(a);
+      } else {
+        if (pl.ragged) spec_stream_kernel<uint16_t, true, false><<<grid, block, pl.smem, st>>>(a);
+        else spec_stream_kernel<uint16_t, false, false><<<grid, block, pl.smem, st>>>(a);
+      }
+    }
+    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return SPEC_OK;
+  }
   // the row kernel is a programmatic dependent launch: it may be scheduled
   // while the segment kernel's last CTAs finish, and waits in its prologue
   cudaLaunchAttribute attr[1];
@@ -2679,14 +3449,15 @@ spec_status spec_verify(const void* target_logits, const void* draft_logits, con
   if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SPEC_ERR_INVALID_ARG;
   if (!p->greedy && (!draft_logits || !uniforms)) return SPEC_ERR_INVALID_ARG;
   if (!workspace_ok(p, pl)) return SPEC_ERR_INVALID_ARG;
-  DevInfo* di = nullptr;
-  if (!dev_info(&di)) return SPEC_ERR_CUDA;
-  s = plan_launch(p, *di, &pl);
-  if (s != SPEC_OK) return s;
   const int64_t es = pl.esize;
   bool al = aligned16(target_logits) && (p->target_seq_stride * es) % 16 == 0 && (p->target_row_stride * es) % 16 == 0;
   if (!p->greedy)
     al = al && aligned16(draft_logits) && (p->draft_seq_stride * es) % 16 == 0 && (p->draft_row_stride * es) % 16 == 0;
+  pl.aligned = al;
+  DevInfo* di = nullptr;
+  if (!dev_info(&di)) return SPEC_ERR_CUDA;
+  s = plan_launch(p, *di, &pl);
+  if (s != SPEC_OK) return s;
   KArgs a = {};
   a.tgt = target_logits;
   a.drf = draft_logits;
@@ -2741,6 +3512,11 @@ spec_status spec_verify_ragged(const void* target_logits, const void* draft_logi
   pl.nrows = total;  // <= the padded B (2K+1) the workspace was sized for
   pl.ragged = true;
   pl.items = total * pl.nseg;
+  const int64_t es = pl.esize;
+  bool al = aligned16(target_logits) && (p->target_seq_stride * es) % 16 == 0 && (p->target_row_stride * es) % 16 == 0;
+  if (!p->greedy)
+    al = al && aligned16(draft_logits) && (p->draft_seq_stride * es) % 16 == 0 && (p->draft_row_stride * es) % 16 == 0;
+  pl.aligned = al;
   DevInfo* di = nullptr;
   if (!dev_info(&di)) return SPEC_ERR_CUDA;
   s = plan_launch(p, *di, &pl);
@@ -2750,10 +3526,6 @@ spec_status spec_verify_ragged(const void* target_logits, const void* draft_logi
   // pageable source: the copy is staged before this call returns
   if (cudaMemcpyAsync(d_map, map.data(), map.size() * sizeof(int2), cudaMemcpyHostToDevice, st) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  const int64_t es = pl.esize;
-  bool al = aligned16(target_logits) && (p->target_seq_stride * es) % 16 == 0 && (p->target_row_stride * es) % 16 == 0;
-  if (!p->greedy)
-    al = al && aligned16(draft_logits) && (p->draft_seq_stride * es) % 16 == 0 && (p->draft_row_stride * es) % 16 == 0;
   KArgs a = {};
   a.tgt = target_logits;
   a.drf = draft_logits;
@@ -2787,14 +3559,15 @@ spec_status spec_sample_verify(const void* target_logits, const void* draft_logi
       !out_num_accepted)
     return SPEC_ERR_INVALID_ARG;
   if (!workspace_ok(p, pl)) return SPEC_ERR_INVALID_ARG;
-  DevInfo* di = nullptr;
-  if (!dev_info(&di)) return SPEC_ERR_CUDA;
-  s = plan_launch(p, *di, &pl);
-  if (s != SPEC_OK) return s;
   const int64_t es = pl.esize;
   const bool al = aligned16(target_logits) && (p->target_seq_stride * es) % 16 == 0 &&
                   (p->target_row_stride * es) % 16 == 0 && aligned16(draft_logits) &&
                   (p->draft_seq_stride * es) % 16 == 0 && (p->draft_row_stride * es) % 16 == 0;
+  pl.aligned = al;
+  DevInfo* di = nullptr;
+  if (!dev_info(&di)) return SPEC_ERR_CUDA;
+  s = plan_launch(p, *di, &pl);
+  if (s != SPEC_OK) return s;
   KArgs a = {};
   a.tgt = target_logits;
   a.drf = draft_logits;
@@ -2825,12 +3598,13 @@ spec_status spec_sample_draft(const void* draft_logits, const double* uniforms, 
   if (p->B == 0) return SPEC_OK;
   if (!draft_logits || !out_tokens || (!p->greedy && !uniforms)) return SPEC_ERR_INVALID_ARG;
   if (!workspace_ok(p, pl)) return SPEC_ERR_INVALID_ARG;
+  const int64_t es = pl.esize;
+  const bool al = aligned16(draft_logits) && (p->draft_seq_stride * es) % 16 == 0 && (p->draft_row_stride * es) % 16 == 0;
+  pl.aligned = al;
   DevInfo* di = nullptr;
   if (!dev_info(&di)) return SPEC_ERR_CUDA;
   s = plan_launch(p, *di, &pl);
   if (s != SPEC_OK) return s;
-  const int64_t es = pl.esize;
-  const bool al = aligned16(draft_logits) && (p->draft_seq_stride * es) % 16 == 0 && (p->draft_row_stride * es) % 16 == 0;
   KArgs a = {};
   a.tgt = draft_logits;  // unused in sample mode
   a.drf = draft_logits;
