@@ -2648,6 +2648,100 @@ __device__ void stream_record(const KArgs& a, const RowInfo& ri, float m, int ar
   rec->flags = flags;
 }
 
+// The sequence epilogue of a sampling call whose rows all stored their kept
+// lists (the streaming kernel's top-k rows): the records of every row in one
+// round of loads, the accept tests, then the two lists the final draw needs
+// in one more round, both held in shared memory.  The arithmetic is the
+// verify epilogue's.  Falls back to it for lists it does not hold.
+// recs: shared scratch for 128 rows (flags, p_tok, zf, list_len).
+template <typename E>
+__device__ void stream_epilogue(const KArgs& a, int b, int K, int first, Scratch& sm, unsigned char* recs) {
+  const int KS = a.K;
+  const int R = 2 * K + 1;
+  const int tid = threadIdx.x;
+  if (R > kThreads) {
+    verify_epilogue<E>(a, b, K, first, sm);
+    return;
+  }
+  double* sp = reinterpret_cast<double*>(recs);
+  double* sz = sp + kThreads;
+  int32_t* sf = reinterpret_cast<int32_t*>(sz + kThreads);
+  int32_t* sl = sf + kThreads;
+  if (tid < R) {
+    const spec_row_stat* r = a.rows + first + tid;
+    sp[tid] = __ldcg(&r->p_tok);
+    sz[tid] = __ldcg(&r->zf);
+    sf[tid] = __ldcg(&r->flags);
+    sl[tid] = __ldcg(&r->list_len);
+  }
+  if (tid == 0) {
+    sm.bi[12] = 0;
+    sm.bi[13] = K;
+  }
+  __syncthreads();
+  if (tid < R && sf[tid]) atomicOr(&sm.bi[12], sf[tid]);
+  // keep d_t with probability min(1, tgt/drf):  u * drf < tgt
+  if (tid < K && !(a.u[static_cast<int64_t>(b) * (KS + 1) + tid] * sp[K + 1 + tid] < sp[tid])) atomicMin(&sm.bi[13], tid);
+  __syncthreads();
+  const int fl = sm.bi[12], n = sm.bi[13];
+  const bool resid = n < K;
+  const int rt = n, rd = K + 1 + n;
+  const int lt = sl[rt], ld = resid ? sl[rd] : 0;
+  constexpr int kHalf = kCap / 2;
+  if (!fl && (lt < 0 || ld < 0 || lt > kHalf || ld > kHalf)) {
+    __syncthreads();
+    verify_epilogue<E>(a, b, K, first, sm);
+    return;
+  }
+  int32_t* out = a.out_tokens + static_cast<int64_t>(b) * (KS + 1);
+  if (fl) {
+    for (int t = tid; t <= KS; t += kThreads) out[t] = -1;
+    if (tid == 0) {
+      a.out_n[b] = -1;
+      set_status(a, (fl & kFlagToken) ? SPEC_ERR_TOKEN_RANGE
+                                      : (fl & kFlagTimeout) ? SPEC_ERR_TIMEOUT : SPEC_ERR_NONFINITE);
+    }
+    return;
+  }
+  for (int t = tid; t <= KS; t += kThreads) out[t] = (t < n) ? a.tokens[static_cast<int64_t>(b) * KS + t] : -1;
+  // the two kept lists (index order) the draw needs
+  int32_t* ti = sm.cand_idx;
+  float* tw = sm.cand_val;
+  int32_t* di = sm.cand_idx + kHalf;
+  float* dw = sm.cand_val + kHalf;
+  {
+    const int64_t jt = static_cast<int64_t>(first) + rt, jd = static_cast<int64_t>(first) + rd;
+    for (int i = tid; i < lt + ld; i += kThreads) {
+      if (i < lt) {
+        ti[i] = __ldcg(&a.list_idx[jt * kCap + i]);
+        tw[i] = __ldcg(&a.list_w[jt * kCap + i]);
+      } else {
+        di[i - lt] = __ldcg(&a.list_idx[jd * kCap + (i - lt)]);
+        dw[i - lt] = __ldcg(&a.list_w[jd * kCap + (i - lt)]);
+      }
+    }
+  }
+  __syncthreads();
+  auto drf_w = [&](int x) -> float {
+    int lo = 0, hi = ld;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (di[mid] < x) lo = mid + 1;
+      else hi = mid;
+    }
+    return (lo < ld && di[lo] == x) ? dw[lo] : 0.0f;
+  };
+  const double u = a.u[static_cast<int64_t>(b) * (KS + 1) + K];
+  const float izt = 1.0f / static_cast<float>(sz[rt]), izd = 1.0f / static_cast<float>(resid ? sz[rd] : 1.0);
+  int pos = -1;
+  if (resid) pos = list_ordered_draw(lt, u, sm, [&](int i) { return fmaxf(0.0f, tw[i] * izt - drf_w(ti[i]) * izd); });
+  if (pos < 0) pos = list_ordered_draw(lt, u, sm, [&](int i) { return tw[i]; });
+  if (tid == 0) {
+    out[n] = (pos >= 0) ? ti[pos] : -1;
+    a.out_n[b] = n;
+  }
+}
+
 // RAG: a ragged call; CAND: top-k candidates (else greedy: max and argmax).
 template <typename E, bool RAG, bool CAND>
 __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a) {
@@ -3073,7 +3167,10 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
         hd.last = last ? 1 : 0;
       }
       __syncthreads();
-      if (hd.last) verify_epilogue<E>(a, ri.b, ri.kb, ri.first, sm);
+      if (hd.last) {
+        if (CAND && !a.fused) stream_epilogue<E>(a, ri.b, ri.kb, ri.first, sm, cand);
+        else verify_epilogue<E>(a, ri.b, ri.kb, ri.first, sm);
+      }
     }
     __syncthreads();  // the Scratch and the candidate buffers are free again
   }
