@@ -2502,13 +2502,15 @@ constexpr int kSWV = 192;          // vectors per warp-stage (3 KB)
 constexpr int kSVPL = kSWV / 32;   // vectors per lane and stage
 constexpr int kSNS = 3;            // buffers per warp
 constexpr int kSWCap = 256;        // candidate entries per warp
-constexpr int kSKeys = 512;        // row-end ranking capacity (keys in the Scratch's candidate arrays)
+constexpr int kSKeys = 256;        // row-end ranking capacity (keys in the Scratch's candidate arrays)
+constexpr int kSGroups = 512;      // row-end groups read back (their first vectors, after the keys)
 constexpr size_t kSStage = static_cast<size_t>(kSWV) * 16;
 constexpr size_t kSRing = static_cast<size_t>(kWarps) * kSNS * kSStage;
 constexpr size_t kSCand = static_cast<size_t>(kWarps) * kSWCap * sizeof(uint2);
 static_assert(kCap * sizeof(unsigned long long) <= kSCand, "the general path's sort keys fit the candidate buffers");
 static_assert(kListTable <= sizeof(int32_t) * kCap + sizeof(float) * kCap &&
-                  kSKeys * sizeof(unsigned long long) <= sizeof(int32_t) * kCap + sizeof(float) * kCap,
+                  kSKeys * sizeof(unsigned long long) + kSGroups * sizeof(int32_t) <=
+                      sizeof(int32_t) * kCap + sizeof(float) * kCap,
               "the merge's entry table and the row-end keys fit the Scratch's candidate arrays");
 static_assert(kSK <= kSWV && 4 * kSK <= kSWCap && kSK <= 64, "a warp's first stage and buffer hold k candidates");
 
@@ -2537,9 +2539,24 @@ __host__ __device__ constexpr size_t stream_smem_bytes() {
 // nonzero (a zero key counts for nothing).  Same value on every lane.
 template <int PER, int KB, typename KeyOf>
 __device__ __forceinline__ uint32_t warp_select_key(KeyOf key_of, int need) {
-  uint32_t t = 0;
+  // the bits that every nonzero key shares with the largest are set from the
+  // start: the result lies between the smallest and the largest key
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  int nz = 0;
+#pragma unroll
+  for (int p = 0; p < PER; ++p) {
+    const uint32_t k = key_of(p);
+    if (k) lo = min(lo, k);
+    hi = max(hi, k);
+    nz += k ? 1 : 0;
+  }
+  lo = __reduce_min_sync(FULL, lo);
+  hi = __reduce_max_sync(FULL, hi);
+  if (static_cast<int>(__reduce_add_sync(FULL, static_cast<unsigned>(nz))) < need) return 0u;
+  const int top = 31 - __clz(lo ^ hi);  // highest differing bit (-1: all keys equal)
+  uint32_t t = (top < 0) ? hi : (hi & ~((2u << top) - 1u));
 #pragma unroll 1
-  for (int bit = 31; bit >= 32 - KB; --bit) {
+  for (int bit = min(top, 31); bit >= 32 - KB; --bit) {
     const uint32_t c = t | (1u << bit);
     int n = 0;
 #pragma unroll
@@ -2593,6 +2610,57 @@ __device__ __forceinline__ int warp_buffer_compact(uint2* wc, int n, float f) {
   }
   __syncwarp();
   return out;
+}
+
+// Bitonic sort of 32 R keys held by one warp (key i at lane i / R, slot
+// i % R), descending.
+template <int R>
+__device__ __forceinline__ void warp_sort_keys_desc(unsigned long long (&key)[R]) {
+  const int t = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32 * R; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < R) sort_stage_regs<R>(key, t, k, j);
+      else sort_stage_lanes<R>(key, t, k, j);
+    }
+}
+
+// list_ordered_draw for n <= 64 entries, by one warp (two entries a lane, lane
+// l holding entries 2l and 2l + 1): the smallest i with u R < cumsum(i), the
+// last positive entry on overflow, -1 if R == 0.  Same value on every lane.
+template <typename WF>
+__device__ int warp_list_draw(int n, double u, WF wf) {
+  const int lane = threadIdx.x & 31;
+  float w[2];
+  FF pre[2];
+  FF run = ff(0.0f);
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int i = 2 * lane + g;
+    w[g] = (i < n) ? wf(i) : 0.0f;
+    run = ff_add(run, w[g]);
+    pre[g] = run;
+  }
+  const FF incl = warp_incl_scan_ff(run, lane);
+  const FF excl = ff_sub(incl, run);
+  const FF total = FF{__shfl_sync(FULL, incl.hi, 31), __shfl_sync(FULL, incl.lo, 31)};
+  if (!(total.hi > 0.0f)) return -1;
+  const FF target = ff_from_d(u * ff_to_d(total));
+  int first = INT_MAX, last = -1;
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int i = 2 * lane + g;
+    const FF before = (g == 0) ? excl : ff_add(excl, pre[0]);
+    const FF c = ff_add(excl, pre[g]);
+    if (w[g] > 0.0f) {
+      last = i;
+      if (ff_lt(target, c) && !ff_lt(target, before)) first = min(first, i);
+    }
+  }
+  first = static_cast<int>(__reduce_min_sync(FULL, static_cast<unsigned>(first)));
+  last = static_cast<int>(__reduce_max_sync(FULL, static_cast<unsigned>(last + 1))) - 1;
+  return (first != INT_MAX) ? first : last;
 }
 
 // This warp's part of a row: its stages, the row's whole vectors and their
@@ -2733,9 +2801,23 @@ __device__ void stream_epilogue(const KArgs& a, int b, int K, int first, Scratch
   };
   const double u = a.u[static_cast<int64_t>(b) * (KS + 1) + K];
   const float izt = 1.0f / static_cast<float>(sz[rt]), izd = 1.0f / static_cast<float>(resid ? sz[rd] : 1.0);
+  auto resid_w = [&](int i) { return fmaxf(0.0f, tw[i] * izt - drf_w(ti[i]) * izd); };
+  auto tgt_w = [&](int i) { return tw[i]; };
+  if (lt <= 64) {
+    // one warp: two entries a lane, no block barriers
+    if (threadIdx.x < 32) {
+      int pos = resid ? warp_list_draw(lt, u, resid_w) : -1;
+      if (pos < 0) pos = warp_list_draw(lt, u, tgt_w);
+      if (tid == 0) {
+        out[n] = (pos >= 0) ? ti[pos] : -1;
+        a.out_n[b] = n;
+      }
+    }
+    return;
+  }
   int pos = -1;
-  if (resid) pos = list_ordered_draw(lt, u, sm, [&](int i) { return fmaxf(0.0f, tw[i] * izt - drf_w(ti[i]) * izd); });
-  if (pos < 0) pos = list_ordered_draw(lt, u, sm, [&](int i) { return tw[i]; });
+  if (resid) pos = list_ordered_draw(lt, u, sm, resid_w);
+  if (pos < 0) pos = list_ordered_draw(lt, u, sm, tgt_w);
   if (tid == 0) {
     out[n] = (pos >= 0) ? ti[pos] : -1;
     a.out_n[b] = n;
@@ -2976,10 +3058,13 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
       };
       // a tighter floor: the k-th largest group max over the whole row (at
       // least k groups, so k elements, reach it)
+      // warp 0: the floor f2, then the first vectors of the groups >= f2, packed
+      // (the ranking keys' space is still free)
+      int32_t* gsel = reinterpret_cast<int32_t*>(keys + kSKeys);
       if (!general && warp == 0) {
         float f2 = f;
+        constexpr int PER = kSWCap / 32;
         if (ng <= kSWCap) {
-          constexpr int PER = kSWCap / 32;
           uint32_t key[PER];
 #pragma unroll
           for (int p = 0; p < PER; ++p) {
@@ -2988,15 +3073,30 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
           }
           f2 = fmaxf(f2, key_floor(warp_select_key<PER, KB>([&](int p) { return key[p]; }, ktop)));
         }
-        if (lane == 0) hd.f2 = f2;
+        int n2 = 0;
+        for (int g0i = 0; g0i < ng; g0i += 32) {
+          const int g = g0i + lane;
+          const uint2 ge = (g < ng) ? group_at(g) : make_uint2(0u, 0xff800000u);
+          const bool in = g < ng && __uint_as_float(ge.y) >= f2;
+          const unsigned bm = __ballot_sync(FULL, in);
+          if (in && n2 + __popc(bm & ((1u << lane) - 1u)) < kSGroups)
+            gsel[n2 + __popc(bm & ((1u << lane) - 1u))] = static_cast<int>(ge.x);
+          n2 += __popc(bm);
+        }
+        if (lane == 0) {
+          hd.f2 = f2;
+          hd.nlist = 0;
+          hd.cut = n2;  // groups listed (reused as a count here)
+        }
       }
       __syncthreads();
       if (!general) {
         f = hd.f2;
+        const int ng2 = (hd.cut <= kSGroups) ? hd.cut : 0;  // more: the general path (no keys)
         const float tf = Seg<E>::grid_floor(f);
         // item = (group, vector of the group); the loads of a round go out together
         constexpr int R = 4;
-        for (int base = 0; base < ng * kSVPL; base += R * kThreads) {
+        for (int base = 0; base < ng2 * kSVPL; base += R * kThreads) {
           uint4 x[R];
           int vv[R];
 #pragma unroll
@@ -3004,15 +3104,12 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
             const int it = base + r * kThreads + tid;
             vv[r] = -1;
             x[r] = Seg<E>::neg_inf();
-            if (it < ng * kSVPL) {
+            if (it < ng2 * kSVPL) {
               const int g = it / kSVPL, j = it - g * kSVPL;
-              const uint2 ge = group_at(g);
-              if (__uint_as_float(ge.y) >= f) {
-                const int v = static_cast<int>(ge.x) + j * 32;
-                vv[r] = v;
-                if (v < nw) x[r] = ld_stream(gv + v);
-                else if (v < nv) x[r] = Seg<E>::load_some(grow, v, a.V - v * N);
-              }
+              const int v = gsel[g] + j * 32;
+              vv[r] = v;
+              if (v < nw) x[r] = ld_stream(gv + v);
+              else if (v < nv) x[r] = Seg<E>::load_some(grow, v, a.V - v * N);
             }
           }
 #pragma unroll
@@ -3029,106 +3126,116 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
       __syncthreads();
       const int n = hd.nlist;
       general = general || n > kSKeys || n < 1;
-      unsigned long long* sorted = reinterpret_cast<unsigned long long*>(cand);  // the buffers are read
-      const int kk = min(ktop, n);
+      // warp 0 alone: sort the keys (value desc, index asc) in registers, cut
+      // top-k then top-p with float-float prefix masses, sort the kept set by
+      // index, write it with the record, and draw a sampled row's token
       if (!general) {
-        const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(keys);
-        for (int i = tid; i < n; i += kThreads) {
-          const unsigned long long key = keys[i];
-          int r = 0;
-          int j = 0;
-#pragma unroll 4
-          for (; j + 1 < n; j += 2) {
-            const ulonglong2 p = k2[j >> 1];
-            r += ((p.x > key) ? 1 : 0) + ((p.y > key) ? 1 : 0);
-          }
-          if (j < n) r += (keys[j] > key) ? 1 : 0;
-          if (r < kk) sorted[r] = key;
-        }
-      }
-      __syncthreads();
-      if (!general && warp == 0) {
-        // prefix of the weights in rank order (two entries a lane), the top-p
-        // cut within the top k, and the kept mass
-        float w2[2];
-        FF pre[2];
-        FF run = ff(0.0f);
+        if (warp == 0) {
+          unsigned long long key[2];
+          if (n <= 64) {
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const int i = 2 * lane + g;
-          w2[g] = (i < kk) ? wexp(skey_val(sorted[i]), m, a.c) : 0.0f;
-          run = ff_add(run, w2[g]);
-          pre[g] = run;
-        }
-        const FF incl = warp_incl_scan_ff(run, lane);
-        const FF excl = ff_sub(incl, run);
-        const FF total = FF{__shfl_sync(FULL, incl.hi, 31), __shfl_sync(FULL, incl.lo, 31)};
-        int cut = kk - 1;
-        if (a.top_p < 1.0f) {
-          const FF need = ff_mul(total, a.top_p);
-          int first = INT_MAX;
+            for (int r = 0; r < 2; ++r) {
+              const int i = 2 * lane + r;
+              key[r] = (i < n) ? keys[i] : 0ull;  // zero keys sort last
+            }
+            warp_sort_keys_desc<2>(key);
+          } else {
+            // up to 256 keys: sorted eight a lane, then the first 64 two a lane
+            unsigned long long k8[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const int i = 8 * lane + r;
+              k8[r] = (i < n) ? keys[i] : 0ull;
+            }
+            warp_sort_keys_desc<8>(k8);
+            __syncwarp();
+            if (lane < 8) {
+#pragma unroll
+              for (int r = 0; r < 8; ++r) keys[8 * lane + r] = k8[r];
+            }
+            __syncwarp();
+#pragma unroll
+            for (int r = 0; r < 2; ++r) key[r] = keys[2 * lane + r];
+          }
+          const int kk = min(ktop, n);
+          float w2[2];
+          FF pre[2];
+          FF run = ff(0.0f);
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
             const int i = 2 * lane + g;
-            if (i < kk && !ff_lt(ff_add(excl, pre[g]), need)) first = min(first, i);
+            w2[g] = (i < kk) ? wexp(skey_val(key[g]), m, a.c) : 0.0f;
+            run = ff_add(run, w2[g]);
+            pre[g] = run;
           }
-          first = static_cast<int>(__reduce_min_sync(FULL, static_cast<unsigned>(first)));
-          if (first != INT_MAX) cut = first;
-        }
-        // the prefix at the cut, from the lane that holds it
-        const int hl = cut >> 1;
-        const FF zc = ff_add(excl, pre[cut & 1]);
-        const float zh = __shfl_sync(FULL, zc.hi, hl), zl = __shfl_sync(FULL, zc.lo, hl);
-        if (lane == 0) {
-          hd.cut = cut;
-          hd.zf = FF{zh, zl};
-        }
-      }
-      __syncthreads();
-      if (!general) {
-        // the kept set in index order: an entry's position is the number of
-        // kept entries with a smaller index
-        const int nkeep = hd.cut + 1;
-        const FF zf = hd.zf;
-        int32_t* lidx = a.list_idx + static_cast<int64_t>(row) * kCap;
-        float* lw = a.list_w + static_cast<int64_t>(row) * kCap;
-        int32_t* sidx = sm.cand_idx;  // the keys are read: the list, for the draw
-        float* sw = sm.cand_val;
-        int xi = -1;
-        float xw = 0.0f;
-        int xpos = 0;
-        if (tid < nkeep) {
-          xi = skey_idx(sorted[tid]);
-          xw = wexp(skey_val(sorted[tid]), m, a.c);
-          for (int j = 0; j < nkeep; ++j) xpos += (skey_idx(sorted[j]) < xi) ? 1 : 0;
-          lidx[xpos] = xi;
-          lw[xpos] = xw;
-        }
-        __syncthreads();  // every key is read
-        if (tid < nkeep) {
-          sidx[xpos] = xi;
-          sw[xpos] = xw;
-        }
-        __syncthreads();
-        const unsigned long long ck = sorted[nkeep - 1];
-        const Cut cut{skey_val(ck), skey_idx(ck)};
-        int tok = -1;
-        if (a.mode == kModeSample || (a.fused && !ri.is_target)) {
-          const double u = a.fused ? a.u_draft[ri.b] : a.u[static_cast<int64_t>(ri.b) * a.K + ri.t];
-          const int pos = list_ordered_draw(nkeep, u, sm, [&](int i) { return sw[i]; });
-          tok = (pos >= 0) ? sidx[pos] : -1;
-        }
-        // the kept weight of a token: a search of the kept list (index order)
-        auto wd = [&](int d) {
-          int lo = 0, hi = nkeep;
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sidx[mid] < d) lo = mid + 1;
-            else hi = mid;
+          const FF incl = warp_incl_scan_ff(run, lane);
+          const FF excl = ff_sub(incl, run);
+          const FF total = FF{__shfl_sync(FULL, incl.hi, 31), __shfl_sync(FULL, incl.lo, 31)};
+          int cut = kk - 1;
+          if (a.top_p < 1.0f) {
+            const FF need = ff_mul(total, a.top_p);
+            int first = INT_MAX;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              const int i = 2 * lane + g;
+              if (i < kk && !ff_lt(ff_add(excl, pre[g]), need)) first = min(first, i);
+            }
+            first = static_cast<int>(__reduce_min_sync(FULL, static_cast<unsigned>(first)));
+            if (first != INT_MAX) cut = first;
           }
-          return (lo < nkeep && sidx[lo] == d) ? sw[lo] : 0.0f;
-        };
-        if (tid == 0) stream_record(a, ri, m, argmax, false, cut, zf, nkeep, tok, wd);
+          const int nkeep = cut + 1;
+          // the kept mass and the cut key, from the lane that holds the cut
+          const int hl = cut >> 1;
+          const FF zc = ff_add(excl, pre[cut & 1]);
+          const FF zf = FF{__shfl_sync(FULL, zc.hi, hl), __shfl_sync(FULL, zc.lo, hl)};
+          const unsigned long long ck = __shfl_sync(FULL, (cut & 1) ? key[1] : key[0], hl);
+          const Cut kc{skey_val(ck), skey_idx(ck)};
+          // the kept set by index: (index asc) as a descending sort of its complement
+          unsigned long long ik[2];
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int i = 2 * lane + g;
+            ik[g] = (i < nkeep) ? ((static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(skey_idx(key[g]))) << 32) |
+                                   __float_as_uint(w2[g]))
+                                : 0ull;
+          }
+          warp_sort_keys_desc<2>(ik);
+          int32_t* lidx = a.list_idx + static_cast<int64_t>(row) * kCap;
+          float* lw = a.list_w + static_cast<int64_t>(row) * kCap;
+          int32_t* sidx = sm.cand_idx;  // the keys are in registers: the list, for the draw
+          float* sw = sm.cand_val;
+          __syncwarp();
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int p = 2 * lane + g;
+            if (p < nkeep) {
+              const int xi = static_cast<int>(0xffffffffu - static_cast<uint32_t>(ik[g] >> 32));
+              const float xw = __uint_as_float(static_cast<uint32_t>(ik[g]));
+              lidx[p] = xi;
+              lw[p] = xw;
+              sidx[p] = xi;
+              sw[p] = xw;
+            }
+          }
+          __syncwarp();
+          int tok = -1;
+          if (a.mode == kModeSample || (a.fused && !ri.is_target)) {
+            const double u = a.fused ? a.u_draft[ri.b] : a.u[static_cast<int64_t>(ri.b) * a.K + ri.t];
+            const int pos = warp_list_draw(nkeep, u, [&](int i) { return sw[i]; });
+            tok = (pos >= 0) ? sidx[pos] : -1;
+          }
+          // the kept weight of a token: a search of the kept list (index order)
+          auto wd = [&](int d) {
+            int lo = 0, hi = nkeep;
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (sidx[mid] < d) lo = mid + 1;
+              else hi = mid;
+            }
+            return (lo < nkeep && sidx[lo] == d) ? sw[lo] : 0.0f;
+          };
+          if (lane == 0) stream_record(a, ri, m, argmax, false, kc, zf, nkeep, tok, wd);
+        }
       } else {
         // the exact general path: the row's record says what the stream could
         // not settle (a non-finite row, or a buffer too small for its ties)
