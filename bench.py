@@ -74,6 +74,15 @@ def recorded_traffic(workload):
     return None
 
 
+def verify_kernel_name(w):
+    """The kernels one spec_verify call launches on this workload (rows start on
+    16-byte boundaries here): the one-launch streaming kernel for greedy and
+    top-k <= 64, else the segment kernel and the dependent row kernel."""
+    if w["greedy"] or 0 < w["top_k"] <= 64:
+        return "spec_stream_kernel (one launch per spec_verify call)"
+    return "spec_seg_kernel + spec_row_kernel (one spec_verify call)"
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -222,6 +231,54 @@ def run_reference(args, name):
 
 # ---------------------------------------------------------------------------
 # the GPU arm
+
+def verify_only(name, steps, dev, sv):
+    """Device time of spec_verify alone on another workload: NSETS rotating
+    device input sets (drafts drawn once per set), `steps` timed calls after
+    three warm-up calls, each bracketed by CUDA events on the launching stream."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    base = workloads.CONFIGS[name]
+    sets = []
+    for s in range(NSETS):
+        w = workloads.make(name, seed=base.seed + 17 * s)
+        conv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)) if w["dtype"] == "bf16" \
+            else torch.from_numpy
+        st = dict(tgt=conv(w["target"]).to(dev), drf=conv(w["draft"]).to(dev),
+                  ud=torch.from_numpy(w["u_draft"]).to(dev), uv=torch.from_numpy(w["u_verify"]).to(dev))
+        prm = dict(temperature=w["temperature"], top_k=w["top_k"], top_p=w["top_p"], greedy=w["greedy"])
+        st["tok"] = sv.spec_sample_draft(st["drf"], None if w["greedy"] else st["ud"], **prm)
+        sets.append(st)
+    B, K, V = w["B"], w["K"], w["V"]
+    dt_code = sv.SPEC_BF16 if w["dtype"] == "bf16" else sv.SPEC_F32
+    ws = torch.zeros(sv.spec_verify_workspace_size(B, K, V, dt_code, w["greedy"]), dtype=torch.uint8, device=dev)
+    out_t = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def verify(s):
+        st = sets[s]
+        sv.spec_verify(st["tgt"], None if w["greedy"] else st["drf"], st["tok"], None if w["greedy"] else st["uv"],
+                       out_tokens=out_t, out_num_accepted=out_n, ws=ws, **prm)
+
+    for j in range(3):
+        verify(j % NSETS)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for j in range(steps):
+        ev[j][0].record(stream)
+        verify(j % NSETS)
+        ev[j][1].record(stream)
+    torch.cuda.synchronize(dev)
+    avg_us = sum(a.elapsed_time(b) for a, b in ev) / steps * 1e3
+    rows = rows_per_step(w)[1]
+    nbytes = rows * V * esize(w)
+    peak, _ = measured_peaks()
+    gbs = nbytes / (avg_us / 1e6) / 1e9
+    del sets, ws
+    torch.cuda.empty_cache()
+    return {"workload": workload_desc(name, w), "avg_us": avg_us, "rows": rows, "bytes": nbytes, "gbs": gbs,
+            "frac": gbs / peak, "rows_per_s": rows / (avg_us / 1e6), "steps": steps}
+
 
 def run_gpu(args, name):
     import torch
@@ -390,6 +447,13 @@ def run_gpu(args, name):
     hist_us = h0.elapsed_time(h1) * 1e3 / nh
     hist_ok = int(hist.sum().item()) == B * (nh + 3)
 
+    # spec_verify alone on the other bandwidth-sized workloads (not part of the step)
+    others = {}
+    if rank == 0 and world == 1 and not args.no_others:
+        for o in ("c3", "c4", "c4_bf16", "c5"):
+            if o != name:
+                others[o] = verify_only(o, 50, dev, sv)
+
     base_cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base_cpu = cpu_baseline(host_first, os.cpu_count() or 1)
@@ -418,13 +482,15 @@ def run_gpu(args, name):
                                                       / max(1, int(hist[:K + 1].sum().item())))}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
-                         "kernel": "spec_seg_kernel + spec_row_kernel (one spec_verify call)",
+                         "kernel": verify_kernel_name(w),
                          "peak_kind": peak_kind},
             "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "steps": e2e_steps},
             "gpu_launches": int(r["launches"]),
             "clocks": {k: r["clocks"][k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
         }
+        if others:
+            line["verify_other_workloads"] = others
         if note:
             line["clocks"]["note"] = note
         if base_cpu is not None:
@@ -579,6 +645,7 @@ def main():
     ap.add_argument("--workload", default="c5", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="skip the spec_verify-only lines of the other workloads")
     ap.add_argument("--decode", action="store_true", help="decode-loop line instead of the verify line")
     ap.add_argument("--sweep-k", action="store_true", help="verify time vs K and the latency model")
     args = ap.parse_args()

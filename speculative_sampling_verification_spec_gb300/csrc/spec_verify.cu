@@ -7,32 +7,35 @@
 // the FDE Interviews breakdown of that paper, section "01 The paper in one
 // minute".
 //
-// Design (one launch per call; no thread block ever waits for another):
-//   * Every vocabulary row the call reads is cut into equal segments of at
-//     most 12 K bf16 / 6 K fp32 elements (24 KB), one CTA per segment.  Each
-//     thread issues its sixteen 16-byte loads at once (64 KB in flight per CTA,
-//     every warp load 512 contiguous bytes) and keeps the values in registers:
-//     each byte of a row is read from HBM once and every later pass over the
-//     segment reads registers.
-//   * Per segment: max (NaN-propagating) and first argmax; the normaliser
-//     relative to the segment max when the row needs the full sum (no filter,
-//     or top-p without top-k); for top-k / top-p a candidate superset: theta =
-//     the n0-th largest of the 256 per-thread maxima, so that at least n0 of
-//     the segment's elements -- among them its top n0 -- lie at or above it,
-//     and every finite element >= theta goes to the segment's candidate list.
-//   * The CTA that finishes a row's last segment (tagged atomic ticket) merges
-//     the segment records: row max and argmax, normaliser (float-float, each
-//     segment rescaled to the row max) and the candidate pool, which is sorted
-//     by (logit desc, index asc) and cut: top-k exactly (each segment kept its
-//     own top-k), top-p when the cut value is >= every segment's theta (nothing
-//     a segment left out can then be kept).  Otherwise -- a pool overflow or a
-//     failed check -- the exact general path runs over the row in global
-//     memory: an 8-probe bracket search over order-preserving keys, ending in
-//     an on-chip sort or a tie cut by index.
-//   * The row record (normaliser, cut, draft-token probability, the kept set in
-//     index order) goes to the caller's workspace; the CTA that finishes a
-//     sequence's last row (second ticket) runs the accept tests and the one
-//     final draw for that sequence.
+// Two paths, picked per call on the host; neither has a thread block wait for
+// another (completion is detected by self-resetting counters, never by
+// spinning).
+//
+//   * spec_stream_kernel, one launch per call: rows whose starts are 16-byte
+//     aligned, greedy or top-k with k <= 64.  A persistent grid of four
+//     128-thread CTAs per SM takes whole rows in order.  Each warp keeps a ring
+//     of bulk-copy buffers full (across row boundaries) and reduces its
+//     stages to a running max and first argmax; top-k also keeps the lane
+//     groups (six 16-byte vectors of a stage) whose max reaches a rising
+//     threshold, since a row's top k elements lie in its k largest groups.
+//     At the row end the largest groups are read back, one warp sorts the
+//     candidates, cuts top-k then top-p, and writes the kept set (index order)
+//     and the row record; the CTA that completes a sequence runs its accept
+//     tests and final draw.  Rows it cannot settle (ties past its buffers,
+//     non-finite values) take the exact general path below.
+//   * spec_seg_kernel + spec_row_kernel, two launches: everything else (no
+//     filter, top-p alone, top-k > 64, unaligned rows).  The segment kernel
+//     streams 24 KB segments of every row (max, first argmax, the normaliser
+//     where the row needs the full sum, a candidate list above a floor); the
+//     row kernel, a programmatic dependent launch, merges each row's segment
+//     records and lists, sorts and cuts the pool (top-k exactly, top-p when
+//     the cut lies above every segment's floor), and otherwise runs the exact
+//     general path over the row in global memory: an 8-probe bracket search
+//     over order-preserving keys, ending in an on-chip sort or a tie cut by
+//     index.  The CTA that completes a sequence runs its epilogue.
+//
+// Both write the same row records (normaliser, cut, draft-token probability,
+// the kept set in index order) to the caller's workspace.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -253,7 +256,7 @@ __device__ __forceinline__ float wexp(float l, float m, float c) { return ex2f((
 
 // ---------------------------------------------------------------------------
 // float-float ("double-single") sums.  GB300 runs FP64 at a small fraction of
-// its FP32 rate, so running totals, prefix sums and cluster reductions keep a
+// its FP32 rate, so running totals, prefix sums and block reductions keep a
 // (hi, lo) pair of floats: Knuth's TwoSum for additions and an FMA-based
 // TwoProduct for scaling give ~48-bit significands on the FP32 pipes.  Doubles
 // appear only in single-thread spots (the accept test, record fields).
@@ -806,7 +809,7 @@ __device__ int cta_ordered_compact(const RowCtx<E>& rc, Scratch& sm, P pred, Emi
   return total;
 }
 
-// ---- rank-0 helpers over the gathered candidate list -------------------------
+// ---- helpers over the gathered candidate list --------------------------------
 
 __device__ __forceinline__ unsigned long long sort_key(float v, int idx) {
   return (static_cast<unsigned long long>(okey32(v)) << 32) | (0xffffffffu - static_cast<uint32_t>(idx));
@@ -945,8 +948,8 @@ __device__ Bracket bracket_search(const RowCtx<E>& rc, Scratch& sm, Local& C, bo
   return br;
 }
 
-// Gather every element >= lo_val (and kept by rcut) into rank 0's candidate
-// list, in index order; returns the cluster count on every CTA.
+// Gather every element >= lo_val (and kept by rcut) into the candidate
+// list, in index order; returns the count on every thread.
 template <typename E>
 __device__ int gather_candidates(const RowCtx<E>& rc, Scratch& sm, Local& C, float lo_val, bool restricted,
                                  Cut rcut) {
@@ -1066,7 +1069,7 @@ __device__ CutResult sort_and_cut(float m, float c, const int32_t* idx, const fl
 }
 
 // Tie cut: index of the c-th (1-based) element equal to tie_val (and kept by
-// rcut), in index order across the cluster.  Same value on every CTA.
+// rcut), in index order over the row.  Same value on every thread.
 template <typename E>
 __device__ int tie_locate(const RowCtx<E>& rc, Scratch& sm, Local& C, float tie_val, int c, bool restricted,
                           Cut rcut) {
@@ -1125,7 +1128,7 @@ __device__ int tie_locate(const RowCtx<E>& rc, Scratch& sm, Local& C, float tie_
   return idx;
 }
 
-// Count and mass of the elements kept by `cut`, cluster-wide (same on every CTA);
+// Count and mass of the elements kept by `cut` over the row (same on every thread);
 // with write_list and a kept set that fits kCap, the kept set is written in index
 // order to lidx / lw.
 template <typename E>
@@ -1243,8 +1246,8 @@ __device__ void set_status(const KArgs& a, int code) {
 }
 
 // ---------------------------------------------------------------------------
-// final draw from full rows in global memory (no stored kept list): the rank-0
-// CTA of the sequence's last cluster alone, over [0, V).  Residual weights
+// final draw from full rows in global memory (no stored kept list): one CTA
+// (the one that completes the sequence), over [0, V).  Residual weights
 // max(0, tgt(x) - drf(x)) or, without `resid`, target weights.  Returns the token,
 // or -1 if the weights sum to zero.
 
@@ -1325,7 +1328,7 @@ __device__ int global_rows_draw(const KArgs& a, const E* gt, const E* gd, float 
 }
 
 // ---------------------------------------------------------------------------
-// verify epilogue: the rank-0 CTA of the last cluster of sequence b
+// verify epilogue: the CTA that completes sequence b
 
 // Accept test of a fused call's draft token d (K = 1): the token was drawn by
 // the draft row of the same call, so its probabilities under both adjusted
@@ -2482,20 +2485,22 @@ __global__ void __launch_bounds__(kThreads, sizeof(E) == 4 ? 8 : 5) spec_row_ker
 //   * Per stage and lane: the max of its six vectors (packed bf16 pairs for
 //     bf16) against the running max; only a new max looks at single elements
 //     (its first index).
-//   * Top-k: a warp keeps every element at or above its threshold in its own
-//     candidate buffer.  The threshold starts at the k-th largest vector
-//     maximum of the warp's first stage (at least k elements lie at or above
-//     it) and rises to the k-th largest buffered value whenever the buffer
-//     passes a high-water mark.  Each such value bounds the row's k-th value
-//     from below, so a warp also takes any higher value another warp
-//     publishes.  A lane whose six vectors all lie below the threshold does no
-//     more work for the stage.
-//   * Row end: the buffered values at or above the largest per-warp k-th
-//     value are ranked in shared memory (value desc, index asc); the first k,
-//     then the top-p prefix within them, are the kept set, written in index
-//     order with the row record.  Ties or a buffer too small for a stage send
-//     the row to the exact general path.  The CTA that completes a sequence (a
-//     counter) runs its accept tests and final draw.
+//   * Top-k works on groups: a lane's six vectors of one stage.  A row's top k
+//     elements lie in the k groups with the largest maxima (k elements reach
+//     the k-th largest group max), so a warp keeps (group max, group) for
+//     every group whose max reaches its threshold -- one slot per lane, no
+//     element work while streaming.  The threshold starts at the k-th largest
+//     vector maximum of the warp's first stage and rises to the k-th largest
+//     buffered group max whenever the buffer passes a high-water mark; every
+//     such value bounds the row's k-th element from below, so a warp also
+//     takes any higher value another warp publishes.
+//   * Row end: the k-th largest group max over the whole row, f2; the groups
+//     at or above it are read back from the row (one round of loads), their
+//     elements >= f2 ranked by one warp in registers (value desc, index asc);
+//     the first k, then the top-p prefix within them, are the kept set,
+//     written in index order with the row record.  Ties or a buffer too small
+//     for a stage send the row to the exact general path.  The CTA that
+//     completes a sequence (a counter) runs its accept tests and final draw.
 
 constexpr int kSK = 64;            // largest top-k the streaming kernel collects
 constexpr int kSWV = 192;          // vectors per warp-stage (3 KB)
