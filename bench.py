@@ -56,18 +56,26 @@ def workload_desc(name, w):
         else "%s: %s, Gaussian synthetic logits" % (name, cfg.describe())
 
 
+def kernel_source_sha():
+    """SHA-256 over the library's CUDA sources (csrc/, in name order)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "speculative_sampling_verification_spec_gb300", "csrc", "*"))):
+        if p.endswith((".cu", ".cuh", ".h")):
+            with open(p, "rb") as f:
+                h.update(os.path.basename(p).encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
 def recorded_traffic(workload):
     """DRAM bytes (read + write) of one spec_verify call on this workload, as an
     ncu capture recorded them in profiles/traffic.json -- only while the kernel
-    source is the one that was captured (else None)."""
-    import hashlib
+    sources are the ones that were captured (else None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
-        src = os.path.join(ROOT, "speculative_sampling_verification_spec_gb300", "csrc", "spec_verify.cu")
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-        if rec.get("source_sha256") == sha and workload in rec.get("verify_bytes_per_call", {}):
+        if rec.get("source_sha256") == kernel_source_sha() and workload in rec.get("verify_bytes_per_call", {}):
             return float(rec["verify_bytes_per_call"][workload])
     except Exception:
         pass
