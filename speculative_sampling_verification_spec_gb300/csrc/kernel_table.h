@@ -10,9 +10,11 @@ const void* seg_f32(bool rag);
 const void* row_f32(bool rag);
 const void* seg_bf16(bool rag);
 const void* row_bf16(bool rag);
-// the one-launch streaming kernel: greedy; top-k candidate groups
+// the one-launch streaming kernel: greedy; top-p; top-k candidate groups
 const void* stream_f32_greedy();
 const void* stream_bf16_greedy();
+const void* stream_f32_topp();
+const void* stream_bf16_topp();
 const void* stream_f32_k();
 const void* stream_bf16_k();
 

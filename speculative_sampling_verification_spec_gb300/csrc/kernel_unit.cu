@@ -1,8 +1,9 @@
 // kernel_unit.cu -- one group of libspecverify's kernels, chosen by SPECV_UNIT
 // at compile time, so that the groups compile in parallel:
 //   1, 2   segment + row kernels, fp32 / bf16
-//   3, 4   streaming kernel without candidates (greedy), fp32 / bf16
-//   5, 6   streaming kernel with top-k candidate groups, fp32 / bf16
+//   3, 4   streaming kernel: greedy, and top-p (candidate groups and the
+//          normaliser), fp32 / bf16
+//   5, 6   streaming kernel: top-k candidate groups, fp32 / bf16
 // Each group's unit defines its entries of kernel_table.h; the build links the
 // units into one library.
 #include "spec_kernels.cuh"
@@ -14,9 +15,9 @@
 
 namespace specv_units {
 namespace {
-template <typename E, bool CAND>
+template <typename E, int MODE>
 const void* stream_ptr() {
-  return reinterpret_cast<const void*>(&spec_stream_kernel<E, CAND>);
+  return reinterpret_cast<const void*>(&spec_stream_kernel<E, MODE>);
 }
 }  // namespace
 
@@ -39,13 +40,15 @@ const void* row_bf16(bool rag) {
              : reinterpret_cast<const void*>(&spec_row_kernel<uint16_t, false>);
 }
 #elif SPECV_UNIT == 3
-const void* stream_f32_greedy() { return stream_ptr<float, false>(); }
+const void* stream_f32_greedy() { return stream_ptr<float, kSMGreedy>(); }
+const void* stream_f32_topp() { return stream_ptr<float, kSMTopP>(); }
 #elif SPECV_UNIT == 4
-const void* stream_bf16_greedy() { return stream_ptr<uint16_t, false>(); }
+const void* stream_bf16_greedy() { return stream_ptr<uint16_t, kSMGreedy>(); }
+const void* stream_bf16_topp() { return stream_ptr<uint16_t, kSMTopP>(); }
 #elif SPECV_UNIT == 5
-const void* stream_f32_k() { return stream_ptr<float, true>(); }
+const void* stream_f32_k() { return stream_ptr<float, kSMTopK>(); }
 #elif SPECV_UNIT == 6
-const void* stream_bf16_k() { return stream_ptr<uint16_t, true>(); }
+const void* stream_bf16_k() { return stream_ptr<uint16_t, kSMTopK>(); }
 #endif
 
 }  // namespace specv_units

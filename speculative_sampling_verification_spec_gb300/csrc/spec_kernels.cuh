@@ -1752,10 +1752,70 @@ __device__ void row_merge(const KArgs& a, int row, Scratch& sm, SortBuf sb, int3
 }
 
 // Row end: exact cut from the pool (or the general path), record, draw.
+// The end of a row once its cut is known: the draw of a sampled row (and of
+// the draft row of a fused call) from the kept list, or by a scan of the row
+// when none is stored, then the row record with the draft token's adjusted
+// probability (its own logit read back).  The whole CTA.
+template <typename E>
+__device__ void row_tail(const KArgs& a, const RowInfo& ri, const E* grow, Scratch& sm, float m, int argmax, bool bad,
+                         Cut cut, FF zf, int list_len) {
+  const int tid = threadIdx.x;
+  spec_row_stat* rec = a.rows + ri.job;
+  int32_t* lidx = a.list_idx + static_cast<int64_t>(ri.job) * kCap;
+  float* lw = a.list_w + static_cast<int64_t>(ri.job) * kCap;
+  // sample mode (and the draft row of a fused call): draw this row's token
+  const bool draws = a.mode == kModeSample || (a.fused && !ri.is_target);
+  if (draws) {
+    const double u = a.greedy ? 0.0 : a.fused ? a.u_draft[ri.b] : a.u[static_cast<int64_t>(ri.b) * a.K + ri.t];
+    int tok;
+    if (bad) {
+      tok = -1;
+    } else if (a.greedy) {
+      tok = argmax;
+    } else if (list_len >= 0) {
+      __syncthreads();
+      const int pos = list_ordered_draw(list_len, u, sm, [&](int i) { return __ldcg(&lw[i]); });
+      tok = (pos >= 0) ? __ldcg(&lidx[pos]) : -1;
+    } else {
+      tok = global_rows_draw<E>(a, grow, grow, m, m, cut, cut, 1.0f, 1.0f, false, u, sm);
+    }
+    if (tid == 0) {
+      if (a.fused) a.out_draft[ri.b] = tok;
+      else a.out_tokens[static_cast<int64_t>(ri.b) * a.K + ri.t] = tok;
+      rec->token = tok;
+    }
+  }
+
+  // row record
+  if (tid == 0) {
+    int flags = 0;
+    if (bad) flags |= kFlagNonfinite;
+    double p_tok = 0.0;
+    if (a.mode == kModeVerify && ri.t < ri.kb && !a.fused) {  // fused: the epilogue computes it
+      const int d = a.tokens[static_cast<int64_t>(ri.b) * a.K + ri.t];
+      if (d < 0 || d >= a.V) {
+        flags |= kFlagToken;
+      } else if (!bad && !a.greedy) {
+        const float ld = Fmt<E>::at_global(grow, d);
+        // same weight as the kept list and the normaliser use
+        if (cut.keep(ld, d) && ld > -INFINITY) p_tok = static_cast<double>(wexp(ld, m, a.c)) / ff_to_d(zf);
+      }
+    }
+    rec->zf = ff_to_d(zf);
+    rec->p_tok = p_tok;
+    rec->m = m;
+    rec->tau_val = cut.tv;
+    rec->tau_idx = cut.ti;
+    rec->argmax = argmax;
+    rec->list_len = list_len;
+    rec->flags = flags;
+    if (a.mode == kModeSample && bad) set_status(a, SPEC_ERR_NONFINITE);
+  }
+}
+
 template <typename E>
 __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scratch& sm, Local& C, SortBuf sb,
                            int32_t* pool_idx, float* pool_val) {
-  const int tid = threadIdx.x;
   // first the pool of every segment list's head: as many entries as a 256-key
   // (top-k) or 512-key (top-p: the nucleus may be long) register sort holds
   const int row = ri.job;
@@ -1776,7 +1836,6 @@ __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scr
   const float theta = sm.row_theta;
   __syncthreads();
 
-  spec_row_stat* rec = a.rows + ri.job;
   int32_t* lidx = a.list_idx + static_cast<int64_t>(ri.job) * kCap;
   float* lw = a.list_w + static_cast<int64_t>(ri.job) * kCap;
   const bool use_k = a.top_k > 0 && a.top_k < a.V;
@@ -1837,54 +1896,7 @@ __device__ void row_finish(const KArgs& a, const RowInfo& ri, const E* grow, Scr
     if (!done) general_cut<E>(a, rg, sm, C, sb, z, &cut, &zf, &list_len, lidx, lw);
   }
 
-  // sample mode (and the draft row of a fused call): draw this row's token
-  const bool draws = a.mode == kModeSample || (a.fused && !ri.is_target);
-  if (draws) {
-    const double u = a.greedy ? 0.0 : a.fused ? a.u_draft[ri.b] : a.u[static_cast<int64_t>(ri.b) * a.K + ri.t];
-    int tok;
-    if (bad) {
-      tok = -1;
-    } else if (a.greedy) {
-      tok = argmax;
-    } else if (list_len >= 0) {
-      __syncthreads();
-      const int pos = list_ordered_draw(list_len, u, sm, [&](int i) { return __ldcg(&lw[i]); });
-      tok = (pos >= 0) ? __ldcg(&lidx[pos]) : -1;
-    } else {
-      tok = global_rows_draw<E>(a, grow, grow, m, m, cut, cut, 1.0f, 1.0f, false, u, sm);
-    }
-    if (tid == 0) {
-      if (a.fused) a.out_draft[ri.b] = tok;
-      else a.out_tokens[static_cast<int64_t>(ri.b) * a.K + ri.t] = tok;
-      rec->token = tok;
-    }
-  }
-
-  // row record
-  if (tid == 0) {
-    int flags = 0;
-    if (bad) flags |= kFlagNonfinite;
-    double p_tok = 0.0;
-    if (a.mode == kModeVerify && ri.t < ri.kb && !a.fused) {  // fused: the epilogue computes it
-      const int d = a.tokens[static_cast<int64_t>(ri.b) * a.K + ri.t];
-      if (d < 0 || d >= a.V) {
-        flags |= kFlagToken;
-      } else if (!bad && !a.greedy) {
-        const float ld = Fmt<E>::at_global(grow, d);
-        // same weight as the kept list and the normaliser use
-        if (cut.keep(ld, d) && ld > -INFINITY) p_tok = static_cast<double>(wexp(ld, m, a.c)) / ff_to_d(zf);
-      }
-    }
-    rec->zf = ff_to_d(zf);
-    rec->p_tok = p_tok;
-    rec->m = m;
-    rec->tau_val = cut.tv;
-    rec->tau_idx = cut.ti;
-    rec->argmax = argmax;
-    rec->list_len = list_len;
-    rec->flags = flags;
-    if (a.mode == kModeSample && bad) set_status(a, SPEC_ERR_NONFINITE);
-  }
+  row_tail<E>(a, ri, grow, sm, m, argmax, bad, cut, zf, list_len);
 }
 
 // ---------------------------------------------------------------------------
@@ -2513,6 +2525,9 @@ constexpr int kSNS = 3;            // buffers per warp
 constexpr int kSWCap = 256;        // candidate entries per warp
 constexpr int kSKeys = 256;        // row-end ranking capacity (keys in the Scratch's candidate arrays)
 constexpr int kSGroups = 512;      // row-end groups read back (their first vectors, after the keys)
+constexpr int kSPKeep = 160;       // top-p: groups a warp keeps when its buffer is cut
+constexpr int kSPHwm = kSWCap - 32; // top-p: buffer entries that trigger the cut (a stage adds <= 32)
+constexpr int kSPBuckets = 2048;   // bf16 top-p pool cut: grid points between the floor and the max
 constexpr size_t kSStage = static_cast<size_t>(kSWV) * 16;
 constexpr size_t kSRing = static_cast<size_t>(kWarps) * kSNS * kSStage;
 constexpr size_t kSCand = static_cast<size_t>(kWarps) * kSWCap * sizeof(uint2);
@@ -2522,6 +2537,14 @@ static_assert(kListTable <= sizeof(int32_t) * kCap + sizeof(float) * kCap &&
                       sizeof(int32_t) * kCap + sizeof(float) * kCap,
               "the merge's entry table and the row-end keys fit the Scratch's candidate arrays");
 static_assert(kSK <= kSWV && 4 * kSK <= kSWCap && kSK <= 64, "a warp's first stage and buffer hold k candidates");
+static_assert(kPool * (2 * sizeof(int32_t) + sizeof(unsigned long long)) + kWarps * kSWCap * sizeof(int32_t) <= kSRing,
+              "the top-p row end's pool, sort keys and group list fit the drained stage ring");
+static_assert(kSPKeep < kSPHwm, "a cut buffer has room for the next stage");
+static_assert(kSPBuckets * sizeof(int) <= kPool * sizeof(unsigned long long) && kThreads <= kSPBuckets,
+              "the bf16 pool cut's buckets (then the bitmap's run prefixes) fit the sort-key space");
+
+// What a streaming launch keeps besides the max and first argmax.
+enum : int { kSMGreedy = 0, kSMTopK = 1, kSMTopP = 2 };
 
 struct alignas(128) StreamHdr {
   uint64_t bar[kWarps * kSNS];  // completion of each warp's buffers
@@ -2535,6 +2558,9 @@ struct alignas(128) StreamHdr {
   float f2;                     // row end: the row's k-th largest group max
   int32_t cut;                  // row end: rank of the last kept entry
   FF zf;                        // row end: kept mass
+  FF wz[kWarps];                // top-p row end: each warp's normaliser, relative to its max
+  float wpart[2 * kWarps];      // top-p row end: the warps' partial masses, by round parity
+  int32_t pc[4];                // top-p row end, bf16 pool cut: crossing thread, bucket, count, last index
   int32_t last;                 // this CTA completed the sequence
 };
 
@@ -2619,6 +2645,180 @@ __device__ __forceinline__ int warp_buffer_compact(uint2* wc, int n, float f) {
   }
   __syncwarp();
   return out;
+}
+
+// Slots for `cnt` entries of every lane of a warp from the shared counter
+// *fill: one atomic per warp; returns this lane's first slot (entries in lane
+// order).
+__device__ __forceinline__ int warp_reserve(int* fill, int cnt) {
+  const int lane = threadIdx.x & 31;
+  const int incl = warp_incl_scan_i(cnt, lane);
+  int base = 0;
+  if (lane == 31 && incl > 0) base = atomicAdd(fill, incl);
+  return __shfl_sync(FULL, base, 31) + incl - cnt;
+}
+
+// Top-p row end: the largest key threshold t (top KB bits) such that the
+// weights wt[p] of the entries whose keys key[p] are >= t add up to at least
+// `need` over the whole CTA (every thread holds PER entries; zero keys count
+// for nothing); a value <= lo when even all of them fall short.  Every
+// nonzero key lies in [lo, hi] (lo > 0): the bits those two share are set from
+// the start.  One block barrier a round; the same value on every thread.
+// part: 2 * kWarps floats.
+template <int PER, int KB>
+__device__ uint32_t block_select_mass(const uint32_t (&key)[PER], const float (&wt)[PER], float need, uint32_t lo,
+                                      uint32_t hi, float* part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lo >= hi) return lo;
+  const int top = 31 - __clz(static_cast<int>(lo ^ hi));  // the first bit they differ in
+  uint32_t t = lo & ~((2u << top) - 1u);                 // their shared prefix: <= every key
+#pragma unroll 1
+  for (int bit = top; bit >= 32 - KB; --bit) {
+    const uint32_t c = t | (1u << bit);
+    float s = 0.0f;
+#pragma unroll
+    for (int p = 0; p < PER; ++p) s += (key[p] >= c) ? wt[p] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+    float* pr = part + (bit & 1) * kWarps;  // the round before and after write the other half
+    if (lane == 0) pr[warp] = s;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += pr[w];
+    if (tot >= need) t = c;
+  }
+  return t;
+}
+
+// The value of a bf16 grid point from its 16-bit order key (okey32 >> 16).
+__device__ __forceinline__ float bf16_key_val(uint32_t k16) {
+  const uint32_t k = k16 << 16;
+  return okey32_val((k & 0x80000000u) ? k : (k | 0xffffu));
+}
+
+// bf16 top-p row end: the cut of a pool that holds every element of the row
+// >= floor_v (n entries: pidx, pval), by counting instead of sorting.  The
+// values lie on the bf16 grid, so a bucket (one grid point) weighs its count
+// times the point's weight.  The buckets are walked from the row max down with
+// float-float prefix masses to the first at which the mass reaches top_p * Z;
+// that bucket's elements are taken in index order until it does.  The kept
+// set is written in index order through a bitmap of the row (its position is
+// the number of kept indices below it) when it fits the stored list.  Returns
+// false, having written nothing, when the values span more than kSPBuckets
+// grid points, the row more than 32 * nbm words, or the pool's mass stays
+// below top_p * Z.  cnt: kSPBuckets ints; bm: nbm words.  The whole CTA.
+__device__ bool pool_bucket_cut(int V, float m, float c, float top_p, FF z, int n, const int32_t* pidx,
+                                const float* pval, float floor_v, int* cnt, uint32_t* bm, int nbm, StreamHdr& hd,
+                                Scratch& sm, int32_t* lidx, float* lw, Cut* cut, FF* zf, int* list_len) {
+  const int tid = threadIdx.x;
+  const int khi = static_cast<int>(okey32(m) >> 16), klo = static_cast<int>(okey32(floor_v) >> 16);
+  const int R = khi - klo + 1;  // bucket b: grid point khi - b
+  const int nw = (V + 31) >> 5;
+  if (R < 1 || R > kSPBuckets || nw > nbm) return false;
+  for (int b = tid; b < R; b += kThreads) cnt[b] = 0;
+  for (int w = tid; w < nw; w += kThreads) bm[w] = 0u;
+  if (tid == 0) hd.pc[0] = INT_MAX;
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) atomicAdd(&cnt[khi - static_cast<int>(okey32(pval[i]) >> 16)], 1);
+  __syncthreads();
+  // each thread a run of buckets, the max first
+  const int per = (R + kThreads - 1) / kThreads;
+  const int b0 = min(R, tid * per), b1 = min(R, b0 + per);
+  FF run = ff(0.0f);
+  for (int b = b0; b < b1; ++b) {
+    const int k = cnt[b];
+    if (k) run = ff_add(run, ff_mul(ff(wexp(bf16_key_val(khi - b), m, c)), static_cast<float>(k)));
+  }
+  FF total;
+  const FF excl = block_excl_scan_ff(run, &total, sm);
+  const FF need = ff_mul(z, top_p);
+  if (ff_lt(total, need)) return false;  // the same on every thread
+  // the first thread whose run reaches need walks it: the bucket, then the
+  // elements of that bucket one at a time
+  if (!ff_lt(ff_add(excl, run), need)) atomicMin(&hd.pc[0], tid);
+  __syncthreads();
+  if (tid == hd.pc[0]) {
+    FF x = excl;
+    int bs = -1, js = 0, blast = -1;
+    for (int b = b0; b < b1 && bs < 0; ++b) {
+      const int k = cnt[b];
+      if (!k) continue;
+      blast = b;
+      const float w = wexp(bf16_key_val(khi - b), m, c);
+      const FF y = ff_add(x, ff_mul(ff(w), static_cast<float>(k)));
+      if (!ff_lt(y, need)) {
+        bs = b;
+        for (js = 0; js < k;) {  // the crossing within the bucket (the whole bucket at most)
+          x = ff_add(x, w);
+          ++js;
+          if (!ff_lt(x, need)) break;
+        }
+      } else {
+        x = y;
+      }
+    }
+    if (bs < 0) {
+      // the run's crossing was not met bucket by bucket (a rounding difference
+      // from the scan): the whole of its last nonempty bucket (bucket 0, the
+      // max, is never empty)
+      for (int b = b0 - 1; blast < 0 && b >= 0; --b)
+        if (cnt[b]) blast = b;
+      bs = blast;
+      js = cnt[bs];
+    }
+    hd.pc[1] = bs;
+    hd.pc[2] = js;
+    hd.pc[3] = -1;
+    hd.zf = x;
+  }
+  __syncthreads();
+  const int bs = hd.pc[1], js = hd.pc[2];
+  const float vs = bf16_key_val(khi - bs);
+  const bool part = js < cnt[bs];  // the cut bucket is taken in part: rank its elements by index
+  for (int i = tid; i < n; i += kThreads) {
+    const float v = pval[i];
+    const int x = pidx[i];
+    bool keep = v > vs;
+    if (v == vs) {
+      int r = 0;
+      if (part)
+        for (int q = 0; q < n; ++q) r += (pval[q] == vs && pidx[q] < x) ? 1 : 0;
+      keep = r < js;
+      if (keep) atomicMax(&hd.pc[3], x);
+    }
+    if (keep) atomicOr(&bm[x >> 5], 1u << (x & 31));
+  }
+  __syncthreads();
+  // positions: a prefix count of the bitmap, in runs of words per thread
+  const int wper = (nw + kThreads - 1) / kThreads;
+  const int w0 = min(nw, tid * wper), w1 = min(nw, w0 + wper);
+  int pc = 0;
+  for (int w = w0; w < w1; ++w) pc += __popc(bm[w]);
+  int nkeep;
+  const int pre = block_excl_scan_i(pc, &nkeep, sm);
+  cnt[tid] = pre;  // the buckets are done with
+  __syncthreads();
+  if (nkeep <= kCap) {
+    for (int i = tid; i < n; i += kThreads) {
+      const int x = pidx[i];
+      const int w = x >> 5;
+      const uint32_t below = bm[w] & ((1u << (x & 31)) - 1u);
+      if (!(bm[w] & (1u << (x & 31)))) continue;
+      const int t = w / wper;
+      int pos = cnt[t] + __popc(below);
+      for (int q = t * wper; q < w; ++q) pos += __popc(bm[q]);
+      lidx[pos] = x;
+      lw[pos] = wexp(pval[i], m, c);
+    }
+    *list_len = nkeep;
+  } else {
+    *list_len = -1;
+  }
+  *cut = Cut{vs, hd.pc[3]};
+  *zf = hd.zf;
+  __syncthreads();
+  return true;
 }
 
 // Bitonic sort of 32 R keys held by one warp (key i at lane i / R, slot
@@ -2833,10 +3033,12 @@ __device__ void stream_epilogue(const KArgs& a, int b, int K, int first, Scratch
   }
 }
 
-// CAND: top-k candidate groups (else greedy: the max and first argmax alone).
-template <typename E, bool CAND>
+// MODE: kSMGreedy (the max and first argmax alone), kSMTopK (top-k candidate
+// groups), kSMTopP (candidate groups and the normaliser; top-p alone).
+template <typename E, int MODE>
 __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a) {
   constexpr bool RAG = false;  // ragged calls take the two-kernel path
+  constexpr bool CAND = MODE != kSMGreedy, TOPP = MODE == kSMTopP;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
   StreamHdr& hd = *reinterpret_cast<StreamHdr*>(smem_raw + sizeof(Scratch));
@@ -2850,7 +3052,9 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
   uint2* wc = reinterpret_cast<uint2*>(cand) + warp * kSWCap;  // CAND: this warp's buffer
   const int G = static_cast<int>(gridDim.x);
   const int ktop = a.top_k;
-  const int hwm = max(kSWCap * 5 / 8, 2 * ktop);  // buffer entries that trigger a cut to the top k
+  // buffer entries that trigger a cut, and the groups the cut keeps
+  const int hwm = TOPP ? kSPHwm : max(kSWCap * 5 / 8, 2 * ktop);
+  const int keep = TOPP ? kSPKeep : ktop;
   const int nv = (a.V + N - 1) / N, nw = a.V / N;  // vectors of a row, whole ones
 
   if (lane == 0) {
@@ -2864,13 +3068,16 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
   bool staged = true;   // this warp still uses bulk copies
   int bnext = 0;        // buffer of this warp's next stage
 
-  // lane 0's issue cursor: row ir, its stage ik, buffer ib
+  // lane 0's issue cursor: row ir, its stage ik, buffer ib.  Top-p stops at
+  // the end of row ilim: its row end works in the drained ring.
   int ir = static_cast<int>(blockIdx.x), ik = 0, ib = 0, inflight = 0;
+  int ilim = TOPP ? ir : INT_MAX;
   RowRing ig{0, 0, nullptr};
   if (lane == 0 && ir < a.nrows) ig = row_ring<E, RAG>(a, ir, warp);
   auto top_up = [&]() {
     while (staged && inflight < kSNS && ir < a.nrows) {
       if (ik >= ig.my) {
+        if (ir >= ilim) break;
         ir += G;
         ik = 0;
         if (ir < a.nrows) ig = row_ring<E, RAG>(a, ir, warp);
@@ -2889,6 +3096,11 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
   if (lane == 0) top_up();
 
   for (int row = static_cast<int>(blockIdx.x); row < a.nrows; row += G) {
+    if (TOPP && lane == 0 && ilim < row) {  // the ring is free again: this row's copies
+      fence_proxy_async_smem();  // after the last row end's generic accesses to the ring
+      ilim = row;
+      top_up();
+    }
     const RowInfo ri = decode_job<RAG>(a, row);
     const E* grow = static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off;
     const uint4* gv = reinterpret_cast<const uint4*>(grow);
@@ -2897,6 +3109,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
 
     float rmax = -INFINITY;
     int rarg = INT_MAX;
+    float zm = -INFINITY;   // TOPP: the lane's normaliser z, relative to zm
+    FF z = ff(0.0f);
     float thr = -INFINITY;  // CAND: this warp's threshold (warp-uniform)
     int wn = 0;             // CAND: entries in the warp's buffer
     bool wover = false;     // CAND: the buffer could not take a stage
@@ -2952,6 +3166,27 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
         rarg = (vs + jf * 32 + lane) * N + ef;
       }
       rmax = max_nan(rmax, tm);
+      if constexpr (TOPP) {
+        // the normaliser: the group's sum relative to its max, folded into the
+        // lane's (rescaled when the group holds a new max)
+        if (tm > -INFINITY) {  // false for NaN: such a row takes the general path
+          float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+          for (int j = 0; j < kSVPL; ++j)
+#pragma unroll
+            for (int i = 0; i < N; i += 2) {
+              s0 += wexp(Seg<E>::get(q[j], i), tm, a.c);
+              s1 += wexp(Seg<E>::get(q[j], i + 1), tm, a.c);
+            }
+          const float s = s0 + s1;
+          if (tm > zm) {
+            z = ff_add(ff_mul(z, wexp(zm, tm, a.c)), s);
+            zm = tm;
+          } else {
+            z = ff_add(z, s * wexp(tm, zm, a.c));
+          }
+        }
+      }
 
       if constexpr (CAND) {
         if (!wover) {
@@ -2961,7 +3196,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
           // threshold; the elements are picked out at the row end.
           // The first stage: the k-th largest finite vector maximum (at least
           // k elements reach it).
-          if (k == 0) {
+          if (!TOPP && k == 0) {
             const uint32_t t = warp_select_key<kSVPL, KB>(
                 [&](int j) {
                   const float v = Seg<E>::pw_max(pw[j]);
@@ -2976,7 +3211,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
           // a buffer past its high-water mark is cut to its k largest groups
           // first (k group maxima at or above a value: k elements at or above it)
           if (wn >= hwm) {
-            te = fmaxf(te, warp_buffer_kth<E>(wc, wn, ktop));
+            te = fmaxf(te, warp_buffer_kth<E>(wc, wn, keep));
             wn = warp_buffer_compact(wc, wn, te);
           }
           const bool hot = tm >= te;  // false for NaN
@@ -3012,9 +3247,17 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
     int wa = (rmax == wm) ? rarg : INT_MAX;  // false for NaN
     wa = static_cast<int>(__reduce_min_sync(FULL, static_cast<unsigned>(wa)));
     float wk = -INFINITY;
-    if constexpr (CAND) {
+    if constexpr (CAND && !TOPP) {
       // this warp's k-th buffered value bounds the row's k-th value from below
       if (!wover && wn >= ktop) wk = warp_buffer_kth<E>(wc, wn, ktop);
+    }
+    if constexpr (TOPP) {
+      // the warp's normaliser relative to its max (float-float butterfly)
+      FF wz = (z.hi > 0.0f) ? ff_mul(z, wexp(zm, wm, a.c)) : ff(0.0f);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        wz = ff_add(wz, FF{__shfl_xor_sync(FULL, wz.hi, o), __shfl_xor_sync(FULL, wz.lo, o)});
+      if (lane == 0) hd.wz[warp] = wz;
     }
     if (lane == 0) {
       hd.wmax[warp] = wm;
@@ -3022,7 +3265,10 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
       hd.wkth[warp] = wk;
       hd.wflag[warp] = wover ? kSegOver : 0;
     }
-    if (tid == 0) hd.nlist = 0;
+    if (tid == 0) {
+      hd.nlist = 0;
+      hd.cut = 0;
+    }
     __syncthreads();
     float m = -INFINITY, f = -INFINITY;
     int am = INT_MAX, fl = 0;
@@ -3042,6 +3288,141 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
     if constexpr (!CAND) {
       if (tid == 0)
         stream_record(a, ri, m, argmax, bad, cut_all(), ff(0.0f), -1, bad ? -1 : argmax, [](int) { return 0.0f; });
+    } else if constexpr (TOPP) {
+      // ---- top-p: every element >= f lies in a buffered group.  A tighter
+      // floor f2 >= f is the largest group max such that the maxima of the
+      // groups at or above it alone weigh at least top_p * Z: at least that
+      // mass lies at or above f2, so the nucleus does too.  The elements >= f2
+      // of those groups are read back from the row into a pool (the ring is
+      // drained), sorted (value desc, index asc) and cut where the prefix mass
+      // reaches top_p * Z.
+      int32_t* pidx = reinterpret_cast<int32_t*>(ring);
+      float* pval = reinterpret_cast<float*>(pidx + kPool);
+      unsigned long long* skey = reinterpret_cast<unsigned long long*>(pval + kPool);
+      int32_t* gsel = reinterpret_cast<int32_t*>(skey + kPool);
+      // the row's normaliser: every warp's sum rescaled to the row max, in warp order
+      FF zrow = ff(0.0f);
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w)
+        if (hd.wz[w].hi > 0.0f) zrow = ff_add(zrow, ff_mul(hd.wz[w], wexp(hd.wmax[w], m, a.c)));
+      bool general = bad || (fl & kSegOver) || !(zrow.hi > 0.0f);
+      if (!general) wn = warp_buffer_compact(wc, wn, f);
+      constexpr int PER = kSWCap / 32;
+      uint32_t gkey[PER];
+      float gw[PER];
+#pragma unroll
+      for (int p = 0; p < PER; ++p) {
+        const int i = p * 32 + lane;
+        const bool in = !general && i < wn;
+        const float g = in ? __uint_as_float(wc[i].y) : -INFINITY;
+        gkey[p] = in ? okey32(g) : 0u;
+        gw[p] = in ? wexp(g, m, a.c) : 0.0f;
+      }
+      float f2 = f;
+      if (!general) {  // block-uniform
+        // a small margin: the float sums of the weights may round up
+        const float need = zrow.hi * a.top_p * (1.0f + 0x1p-10f);
+        f2 = fmaxf(f, key_floor(block_select_mass<PER, KB>(gkey, gw, need, okey32(f), okey32(m), hd.wpart)));
+      }
+#pragma unroll
+      for (int p = 0; p < PER; ++p) {
+        const int i = p * 32 + lane;
+        if (!general && i < wn && __uint_as_float(wc[i].y) >= f2) gsel[atomicAdd(&hd.cut, 1)] = static_cast<int>(wc[i].x);
+      }
+      __syncthreads();
+      if (!general) {
+        const int ng2 = hd.cut;
+        const float tf = Seg<E>::grid_floor(f2);
+        // item = (group, vector of the group); the loads of a round go out together
+        constexpr int R = 8;
+        for (int base = 0; base < ng2 * kSVPL; base += R * kThreads) {
+          uint4 x[R];
+          int vv[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const int it = base + r * kThreads + tid;
+            vv[r] = -1;
+            x[r] = Seg<E>::neg_inf();
+            if (it < ng2 * kSVPL) {
+              const int g = it / kSVPL, j = it - g * kSVPL;
+              const int v = gsel[g] + j * 32;
+              vv[r] = v;
+              if (v < nw) x[r] = ld_stream(gv + v);
+              else if (v < nv) x[r] = Seg<E>::load_some(grow, v, a.V - v * N);
+            }
+          }
+          uint32_t mk[R];
+          int cnt = 0;
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            mk[r] = (vv[r] >= 0) ? Seg<E>::ge_mask(x[r], tf) : 0u;
+            cnt += __popc(mk[r]);
+          }
+          int pos = warp_reserve(&hd.nlist, cnt);
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            for (uint32_t b = mk[r]; b; b &= b - 1, ++pos) {
+              const int i = __ffs(b) - 1;
+              if (pos < kPool) {
+                pidx[pos] = vv[r] * N + i;
+                pval[pos] = Seg<E>::get(x[r], i);
+              }
+            }
+        }
+      }
+      __syncthreads();
+      const int n = hd.nlist;
+      general = general || n > kPool || n < 1;
+      if (!general) {
+        int32_t* lidx = a.list_idx + static_cast<int64_t>(row) * kCap;
+        float* lw = a.list_w + static_cast<int64_t>(row) * kCap;
+        Cut kc = cut_all();
+        FF kz = zrow;
+        int list_len = -1;
+        bool done = false;
+        if constexpr (sizeof(E) == 2) {
+          // bf16: by counting (the ring past the pool holds the buckets and the bitmap)
+          int* cnt = reinterpret_cast<int*>(skey);
+          uint32_t* bm = reinterpret_cast<uint32_t*>(gsel);
+          constexpr int kBm = static_cast<int>((kSRing - 2 * kPool * sizeof(int32_t) - kPool * sizeof(unsigned long long)) /
+                                               sizeof(uint32_t));
+          done = pool_bucket_cut(a.V, m, a.c, a.top_p, zrow, n, pidx, pval, Seg<E>::grid_floor(f2), cnt, bm, kBm, hd,
+                                 sm, lidx, lw, &kc, &kz, &list_len);
+        }
+        if (!done) {
+          const CutResult res = sort_and_cut(m, a.c, pidx, pval, n, SortBuf{skey, nullptr}, 0, a.top_p, zrow, sm);
+          if (res.reached) {
+            if (res.nkeep <= kCap) {
+              write_kept_by_index(skey, res.nkeep, m, a.c, lidx, lw, sm);
+              list_len = res.nkeep;
+            }
+            kc = Cut{res.tv, res.ti};
+            kz = res.zf;
+            done = true;
+          }
+        }
+        if (done) row_tail<E>(a, ri, grow, sm, m, argmax, false, kc, kz, list_len);
+        else general = true;  // the pool's mass stays below top_p * Z
+        __syncthreads();
+      }
+      if (general) {
+        // the exact general path, with the row's max, argmax and normaliser
+        if (tid == 0) {
+          SegRec* rec = a.segs + row;
+          rec->m = m;
+          rec->argmax = argmax;
+          rec->z_hi = zrow.hi;
+          rec->z_lo = zrow.lo;
+          rec->theta = -INFINITY;
+          rec->kth = -INFINITY;
+          rec->ncand = 0;
+          rec->flags = (bad ? kSegBad : 0) | kSegOver;
+        }
+        __syncthreads();
+        Local C;
+        const SortBuf sb{reinterpret_cast<unsigned long long*>(cand), reinterpret_cast<uint8_t*>(sm.cand_idx)};
+        row_finish<E>(a, ri, grow, sm, C, sb, reinterpret_cast<int32_t*>(cand), reinterpret_cast<float*>(cand));
+      }
     } else {
       // ---- top-k: the groups whose max is >= f hold every element >= f; their
       // elements >= f are read back from the row (the copies are gone) and
@@ -3122,15 +3503,20 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
               else if (v < nv) x[r] = Seg<E>::load_some(grow, v, a.V - v * N);
             }
           }
+          uint32_t mk[R];
+          int cnt = 0;
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            if (vv[r] < 0) continue;
-            for (uint32_t mk = Seg<E>::ge_mask(x[r], tf); mk; mk &= mk - 1) {
-              const int i = __ffs(mk) - 1;
-              const int pos = atomicAdd(&hd.nlist, 1);
+            mk[r] = (vv[r] >= 0) ? Seg<E>::ge_mask(x[r], tf) : 0u;
+            cnt += __popc(mk[r]);
+          }
+          int pos = warp_reserve(&hd.nlist, cnt);
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            for (uint32_t b = mk[r]; b; b &= b - 1, ++pos) {
+              const int i = __ffs(b) - 1;
               if (pos < kSKeys) keys[pos] = sort_key(Seg<E>::get(x[r], i), vv[r] * N + i);
             }
-          }
         }
       }
       __syncthreads();

@@ -39,8 +39,8 @@ struct DevInfo {
   int max_smem = 0;
   size_t smem_set[8] = {};  // dynamic smem attribute set: [kernel * 4 + ragged * 2 + dtype]
   int per_sm[4] = {};       // resident segment-kernel CTAs per SM: [ragged * 2 + dtype]
-  size_t ssmem_set[4] = {};  // streaming kernel: [top-k * 2 + dtype]
-  int sper_sm[4] = {};       // resident streaming-kernel CTAs per SM, same index
+  size_t ssmem_set[6] = {};  // streaming kernel: [mode * 2 + dtype]
+  int sper_sm[6] = {};       // resident streaming-kernel CTAs per SM, same index
 };
 std::mutex g_mu;
 DevInfo g_dev[64];
@@ -67,7 +67,7 @@ struct Plan {
   bool ragged = false;          // per-sequence draft lengths (the kernels' RAG instantiation)
   bool aligned = false;         // every row start is 16-byte aligned
   bool stream = false;          // the one-launch streaming kernel (else segment + row kernels)
-  bool scand = false;           // its top-k instantiation (else greedy)
+  int smode = kSMGreedy;        // its instantiation: kSMGreedy, kSMTopK, kSMTopP
   int nseg_ws = 0;              // segment records per row the workspace holds
   size_t counter_bytes = 0;
   int64_t nrows = 0, items = 0;
@@ -139,9 +139,10 @@ spec_status make_plan(const spec_params* p, bool verify, Plan* pl) {
 
 const void* seg_fn(bool f32, bool rag) { return f32 ? specv_units::seg_f32(rag) : specv_units::seg_bf16(rag); }
 const void* row_fn(bool f32, bool rag) { return f32 ? specv_units::row_f32(rag) : specv_units::row_bf16(rag); }
-const void* stream_fn(bool f32, bool cand) {
+const void* stream_fn(bool f32, int mode) {
   using namespace specv_units;
-  if (cand) return f32 ? stream_f32_k() : stream_bf16_k();
+  if (mode == kSMTopK) return f32 ? stream_f32_k() : stream_bf16_k();
+  if (mode == kSMTopP) return f32 ? stream_f32_topp() : stream_bf16_topp();
   return f32 ? stream_f32_greedy() : stream_bf16_greedy();
 }
 
@@ -154,23 +155,27 @@ spec_status set_smem(DevInfo& di, int slot, const void* fn, size_t bytes) {
   return SPEC_OK;
 }
 
-// The streaming kernel takes greedy and top-k (k <= kSK) calls whose rows start
-// on 16-byte boundaries, except ragged ones: a persistent grid, as many CTAs as
-// fit at once, one row at a time each (the row record and the kept list go
+// The streaming kernel takes greedy, top-k (k <= kSK, with or without top-p)
+// and top-p calls whose rows start on 16-byte boundaries, except ragged ones: a
+// persistent grid, as many CTAs as fit at once, one row at a time each (the row record and the kept list go
 // where the two-kernel path puts them; its per-row part record is written only
 // for the general path).
 spec_status plan_stream(const spec_params* p, DevInfo& di, Plan* pl) {
   const bool use_k = !p->greedy && p->top_k > 0 && p->top_k < p->V;
-  // top-p alone (and no filter) stays on the two-kernel path: a nucleus longer
-  // than the candidate groups hold would send the row to the general path,
-  // whose passes over the row in global memory cost more than the two kernels
-  if (!pl->aligned || pl->ragged || !(p->greedy || (use_k && p->top_k <= kSK))) return SPEC_OK;
-  const bool cand = !p->greedy;  // greedy: max and argmax; top-k: candidate groups
+  const bool use_p = !p->greedy && p->top_p < 1.0f;
+  // no filter stays on the two-kernel path (the kept set is the whole row)
+  if (!pl->aligned || pl->ragged) return SPEC_OK;
+  int mode;
+  if (p->greedy) mode = kSMGreedy;            // max and argmax
+  else if (use_k && p->top_k <= kSK) mode = kSMTopK;  // candidate groups (top-p within them)
+  else if (use_p && !use_k) mode = kSMTopP;   // candidate groups and the normaliser
+  else return SPEC_OK;
+  const bool cand = mode != kSMGreedy;
   const size_t smem = cand ? stream_smem_bytes<1>() : stream_smem_bytes<0>();
   if (smem > static_cast<size_t>(di.max_smem)) return SPEC_OK;
   const int which = (p->dtype == SPEC_F32) ? 0 : 1;
-  const int slot = (cand ? 2 : 0) + which;
-  const void* fn = stream_fn(which == 0, cand);
+  const int slot = mode * 2 + which;
+  const void* fn = stream_fn(which == 0, mode);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (di.ssmem_set[slot] < smem) {
@@ -189,7 +194,7 @@ spec_status plan_stream(const spec_params* p, DevInfo& di, Plan* pl) {
   }
   const int64_t slots = static_cast<int64_t>(di.sper_sm[slot]) * di.sms;
   pl->stream = true;
-  pl->scand = cand;
+  pl->smode = mode;
   pl->S = p->V;
   pl->nseg = 1;
   pl->items = pl->nrows;
@@ -237,7 +242,7 @@ spec_status launch(const spec_params* p, const Plan& pl, KArgs& a, DevInfo* di) 
   if (pl.clear_counters && cudaMemsetAsync(p->workspace, 0, pl.counter_bytes, st) != cudaSuccess)
     return SPEC_ERR_CUDA;
   if (pl.stream) {
-    const void* fn = stream_fn(p->dtype == SPEC_F32, pl.scand);
+    const void* fn = stream_fn(p->dtype == SPEC_F32, pl.smode);
     void* args[] = {&a};
     if (cudaLaunchKernel(fn, grid, block, args, pl.smem, st) != cudaSuccess) return SPEC_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;

@@ -139,6 +139,10 @@ def _custom(B, K, V, rng, scale=2.0, dtype="f32"):
     dict(V=2000, K=2, B=32, top_p=0.85, scale=0.3),
     dict(V=5000, K=2, B=4, temperature=0.05),
     dict(V=5000, K=2, B=4, temperature=5.0, top_p=0.5),
+    # top-p alone on 16-byte aligned rows: the streaming kernel's nucleus pool
+    dict(V=4096, K=2, B=6, dtype="bf16", temperature=0.8, top_p=0.9),
+    dict(V=12000, K=3, B=5, scale=3.0, top_p=0.7),
+    dict(V=8192, K=2, B=4, dtype="bf16", scale=1.0, top_p=0.95),  # nuclei of hundreds of tokens
     dict(V=4099, K=3, B=5, dtype="bf16", top_k=13, temperature=0.7),
     dict(V=2048, K=4, B=8, greedy=True, dtype="bf16", scale=0.3),   # many exact ties
 ])
