@@ -1996,6 +1996,32 @@ struct Seg<uint16_t> {  // bf16 bits, 8 per vector
     }
     return max_nan(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xffff0000u));
   }
+  // Sum of 2^((x - g) c) over the NV vectors' elements (g: their max, finite),
+  // the weight function's arithmetic (x - g, then times c, rounded to
+  // nearest) on packed f32 pairs
+  template <int NV>
+  __device__ static float zsum(const uint4 (&q)[NV], float g, float c) {
+    uint64_t gg, cc, s = 0ull;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(gg) : "f"(g));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t x = word_of(q[j], w);
+        uint64_t p, d;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "r"(x << 16), "r"(x & 0xffff0000u));
+        asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(p), "l"(gg));
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(d), "l"(cc));
+        float lo, hi;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(d));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(ex2f(lo)), "f"(ex2f(hi)));
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(s), "l"(p));
+      }
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(s));
+    return lo + hi;
+  }
   // NaN-propagating max of the vector, on packed pairs
   __device__ static float vmax(const uint4& q) {
     __nv_bfloat162 a, b, c, d;
@@ -3170,15 +3196,20 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
         // the normaliser: the group's sum relative to its max, folded into the
         // lane's (rescaled when the group holds a new max)
         if (tm > -INFINITY) {  // false for NaN: such a row takes the general path
-          float s0 = 0.0f, s1 = 0.0f;
+          float s;
+          if constexpr (sizeof(E) == 2) {
+            s = Seg<E>::template zsum<kSVPL>(q, tm, a.c);
+          } else {
+            float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-          for (int j = 0; j < kSVPL; ++j)
+            for (int j = 0; j < kSVPL; ++j)
 #pragma unroll
-            for (int i = 0; i < N; i += 2) {
-              s0 += wexp(Seg<E>::get(q[j], i), tm, a.c);
-              s1 += wexp(Seg<E>::get(q[j], i + 1), tm, a.c);
-            }
-          const float s = s0 + s1;
+              for (int i = 0; i < N; i += 2) {
+                s0 += wexp(Seg<E>::get(q[j], i), tm, a.c);
+                s1 += wexp(Seg<E>::get(q[j], i + 1), tm, a.c);
+              }
+            s = s0 + s1;
+          }
           if (tm > zm) {
             z = ff_add(ff_mul(z, wexp(zm, tm, a.c)), s);
             zm = tm;
