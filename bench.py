@@ -84,9 +84,12 @@ def recorded_traffic(workload):
 
 def verify_kernel_name(w):
     """The kernels one spec_verify call launches on this workload (rows start on
-    16-byte boundaries here): the one-launch streaming kernel for greedy and
-    top-k <= 64, else the segment kernel and the dependent row kernel."""
-    if w["greedy"] or 0 < w["top_k"] <= 64:
+    16-byte boundaries here): the one-launch streaming kernel for greedy,
+    top-k <= 64 and top-p alone, else the segment kernel and the dependent row
+    kernel."""
+    V = w["V"]
+    use_k = 0 < w["top_k"] < V
+    if w["greedy"] or (use_k and w["top_k"] <= 64) or (not use_k and w["top_p"] < 1.0):
         return "spec_stream_kernel (one launch per spec_verify call)"
     return "spec_seg_kernel + spec_row_kernel (one spec_verify call)"
 

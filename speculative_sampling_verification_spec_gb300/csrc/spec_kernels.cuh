@@ -2575,18 +2575,17 @@ enum : int { kSMGreedy = 0, kSMTopK = 1, kSMTopP = 2 };
 struct alignas(128) StreamHdr {
   uint64_t bar[kWarps * kSNS];  // completion of each warp's buffers
   float wthr[kWarps];           // published warp thresholds of the current row
-  float wkth[kWarps];           // row end: each warp's k-th buffered value
   float wmax[kWarps];
   int32_t warg[kWarps];
   int32_t wflag[kWarps];        // row end: kSegOver
   int32_t wfill[kWarps];        // entries in each warp's buffer (slots taken by atomics)
   int32_t nlist;                // row end: keys gathered
-  float f2;                     // row end: the row's k-th largest group max
   int32_t cut;                  // row end: rank of the last kept entry
   FF zf;                        // row end: kept mass
   FF wz[kWarps];                // top-p row end: each warp's normaliser, relative to its max
-  float wpart[2 * kWarps];      // top-p row end: the warps' partial masses, by round parity
   int32_t pc[4];                // top-p row end, bf16 pool cut: crossing thread, bucket, count, last index
+  uint32_t rbins[48];           // top-k row end: the radix select's three rounds of 16 bins
+  float wpart[2 * kWarps];      // top-p row end: the warps' partial masses, by round parity
   int32_t last;                 // this CTA completed the sequence
 };
 
@@ -2682,6 +2681,49 @@ __device__ __forceinline__ int warp_reserve(int* fill, int cnt) {
   int base = 0;
   if (lane == 31 && incl > 0) base = atomicAdd(fill, incl);
   return __shfl_sync(FULL, base, 31) + incl - cnt;
+}
+
+// The largest key threshold t (its set bits in the top KB bits) such that the
+// values v[p] of the keys key[p] >= t add up to at least `need` over the
+// whole CTA (every thread holds PER keys; zero keys count for nothing); 0 when
+// even all of them fall short.  Four key bits a round: each round adds the
+// values of the keys that match the bits fixed so far into 16 shared bins by
+// their next digit, and every thread walks the bins from the top digit down.
+// T = int (counts: the need-th largest key).
+// bins: 3 x 16 of T, zero on entry; one block barrier a round; the same value
+// on every thread.
+template <int PER, int KB, typename T>
+__device__ uint32_t block_radix_select(const uint32_t (&key)[PER], const T (&v)[PER], T need, void* bins) {
+  T* bn = static_cast<T*>(bins);
+  uint32_t t = 0;
+  T above = T(0);
+  int r = 0;
+#pragma unroll 1
+  for (int shift = 28; shift >= 32 - KB; shift -= 4, ++r) {
+    T* b = bn + (r % 3) * 16;
+    const uint32_t hm = (shift == 28) ? 0u : (0xffffffffu << (shift + 4));  // the bits fixed so far
+#pragma unroll
+    for (int p = 0; p < PER; ++p)
+      if (key[p] != 0u && (key[p] & hm) == t) atomicAdd(&b[(key[p] >> shift) & 15u], v[p]);
+    __syncthreads();
+    // the bins of round r + 2 were read last in round r - 1
+    if (threadIdx.x < 16) bn[((r + 2) % 3) * 16 + threadIdx.x] = T(0);
+    T acc = above;
+    int ds = -1;
+#pragma unroll 1
+    for (int d = 15; d >= 0; --d) {
+      const T x = b[d];
+      if (acc + x >= need) {
+        ds = d;
+        break;
+      }
+      acc += x;
+    }
+    if (ds < 0) return 0u;  // the same on every thread
+    t |= static_cast<uint32_t>(ds) << shift;
+    above = acc;
+  }
+  return t;
 }
 
 // Top-p row end: the largest key threshold t (top KB bits) such that the
@@ -3277,11 +3319,6 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
     for (int o = 16; o > 0; o >>= 1) wm = max_nan(wm, __shfl_xor_sync(FULL, wm, o));
     int wa = (rmax == wm) ? rarg : INT_MAX;  // false for NaN
     wa = static_cast<int>(__reduce_min_sync(FULL, static_cast<unsigned>(wa)));
-    float wk = -INFINITY;
-    if constexpr (CAND && !TOPP) {
-      // this warp's k-th buffered value bounds the row's k-th value from below
-      if (!wover && wn >= ktop) wk = warp_buffer_kth<E>(wc, wn, ktop);
-    }
     if constexpr (TOPP) {
       // the warp's normaliser relative to its max (float-float butterfly)
       FF wz = (z.hi > 0.0f) ? ff_mul(z, wexp(zm, wm, a.c)) : ff(0.0f);
@@ -3293,13 +3330,13 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
     if (lane == 0) {
       hd.wmax[warp] = wm;
       hd.warg[warp] = wa;
-      hd.wkth[warp] = wk;
       hd.wflag[warp] = wover ? kSegOver : 0;
     }
     if (tid == 0) {
       hd.nlist = 0;
       hd.cut = 0;
     }
+    if (CAND && tid < 48) hd.rbins[tid] = 0u;
     __syncthreads();
     float m = -INFINITY, f = -INFINITY;
     int am = INT_MAX, fl = 0;
@@ -3309,7 +3346,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
     for (int w = 0; w < kWarps; ++w) {
       if (hd.wmax[w] == m) am = min(am, hd.warg[w]);
       fl |= hd.wflag[w];
-      f = fmaxf(f, fmaxf(hd.wthr[w], hd.wkth[w]));
+      f = fmaxf(f, hd.wthr[w]);
     }
     const bool bad = !(m == m) || m == INFINITY || !(m > -INFINITY);
     const int argmax = (am == INT_MAX) ? -1 : am;
@@ -3337,28 +3374,32 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
       for (int w = 0; w < kWarps; ++w)
         if (hd.wz[w].hi > 0.0f) zrow = ff_add(zrow, ff_mul(hd.wz[w], wexp(hd.wmax[w], m, a.c)));
       bool general = bad || (fl & kSegOver) || !(zrow.hi > 0.0f);
-      if (!general) wn = warp_buffer_compact(wc, wn, f);
       constexpr int PER = kSWCap / 32;
       uint32_t gkey[PER];
       float gw[PER];
 #pragma unroll
       for (int p = 0; p < PER; ++p) {
         const int i = p * 32 + lane;
-        const bool in = !general && i < wn;
-        const float g = in ? __uint_as_float(wc[i].y) : -INFINITY;
-        gkey[p] = in ? okey32(g) : 0u;
-        gw[p] = in ? wexp(g, m, a.c) : 0.0f;
+        const float g0v = (!general && i < wn) ? __uint_as_float(wc[i].y) : -INFINITY;
+        const bool in = !general && i < wn && g0v >= f;
+        gkey[p] = in ? okey32(g0v) : 0u;
+        gw[p] = in ? wexp(g0v, m, a.c) : 0.0f;
       }
       float f2 = f;
       if (!general) {  // block-uniform
-        // a small margin: the float sums of the weights may round up
+        // a small margin: the float sums of the weights may round up.  A
+        // bisection (bins of masses would take contended float atomics)
         const float need = zrow.hi * a.top_p * (1.0f + 0x1p-10f);
         f2 = fmaxf(f, key_floor(block_select_mass<PER, KB>(gkey, gw, need, okey32(f), okey32(m), hd.wpart)));
       }
+      {
+        int cnt = 0;
 #pragma unroll
-      for (int p = 0; p < PER; ++p) {
-        const int i = p * 32 + lane;
-        if (!general && i < wn && __uint_as_float(wc[i].y) >= f2) gsel[atomicAdd(&hd.cut, 1)] = static_cast<int>(wc[i].x);
+        for (int p = 0; p < PER; ++p) cnt += (gkey[p] != 0u && okey32_val(gkey[p]) >= f2) ? 1 : 0;
+        int pos = warp_reserve(&hd.cut, cnt);
+#pragma unroll
+        for (int p = 0; p < PER; ++p)
+          if (gkey[p] != 0u && okey32_val(gkey[p]) >= f2) gsel[pos++] = static_cast<int>(wc[p * 32 + lane].x);
       }
       __syncthreads();
       if (!general) {
@@ -3459,61 +3500,39 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
       // elements >= f are read back from the row (the copies are gone) and
       // ranked (value desc, index asc)
       unsigned long long* keys = reinterpret_cast<unsigned long long*>(sm.cand_idx);
-      bool general = bad || (fl & kSegOver);
-      if (!general) {
-        // this warp's groups >= f, packed to the front of its buffer
-        wn = warp_buffer_compact(wc, wn, f);
-        if (lane == 0) hd.wflag[warp] = wn;
-      }
-      __syncthreads();
-      int g0[kWarps + 1];
-      g0[0] = 0;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) g0[w + 1] = g0[w] + (general ? 0 : hd.wflag[w]);
-      const int ng = g0[kWarps];
-      const uint2* allc = reinterpret_cast<const uint2*>(cand);
-      auto group_at = [&](int g) {
-        int w = 0;
-#pragma unroll
-        for (int x = 1; x < kWarps; ++x) w = (g >= g0[x]) ? x : w;
-        return allc[w * kSWCap + (g - g0[w])];
-      };
-      // a tighter floor: the k-th largest group max over the whole row (at
-      // least k groups, so k elements, reach it)
-      // warp 0: the floor f2, then the first vectors of the groups >= f2, packed
-      // (the ranking keys' space is still free)
       int32_t* gsel = reinterpret_cast<int32_t*>(keys + kSKeys);
-      if (!general && warp == 0) {
-        float f2 = f;
-        constexpr int PER = kSWCap / 32;
-        if (ng <= kSWCap) {
-          uint32_t key[PER];
+      bool general = bad || (fl & kSegOver);
+      // every group whose max is >= f is buffered, so the k-th largest
+      // buffered group max is the row's: a tighter floor f2 (at least k groups,
+      // so k elements, reach it); then the groups >= f2 are listed
+      constexpr int PER = kSWCap / 32;
+      uint32_t gkey[PER];
+      int gone[PER];
 #pragma unroll
-          for (int p = 0; p < PER; ++p) {
-            const int g = p * 32 + lane;
-            key[p] = (g < ng) ? okey32(__uint_as_float(group_at(g).y)) : 0u;
+      for (int p = 0; p < PER; ++p) {
+        const int i = p * 32 + lane;
+        const float g = (!general && i < wn) ? __uint_as_float(wc[i].y) : -INFINITY;
+        const bool in = !general && i < wn && g >= f;
+        gkey[p] = in ? okey32(g) : 0u;
+        gone[p] = in ? 1 : 0;
+      }
+      float f2 = f;
+      if (!general) f2 = fmaxf(f, key_floor(block_radix_select<PER, KB, int>(gkey, gone, ktop, hd.rbins)));
+      {
+        int cnt = 0;
+#pragma unroll
+        for (int p = 0; p < PER; ++p) cnt += (gkey[p] != 0u && okey32_val(gkey[p]) >= f2) ? 1 : 0;
+        int pos = warp_reserve(&hd.cut, cnt);
+#pragma unroll
+        for (int p = 0; p < PER; ++p)
+          if (gkey[p] != 0u && okey32_val(gkey[p]) >= f2) {
+            if (pos < kSGroups) gsel[pos] = static_cast<int>(wc[p * 32 + lane].x);
+            ++pos;
           }
-          f2 = fmaxf(f2, key_floor(warp_select_key<PER, KB>([&](int p) { return key[p]; }, ktop)));
-        }
-        int n2 = 0;
-        for (int g0i = 0; g0i < ng; g0i += 32) {
-          const int g = g0i + lane;
-          const uint2 ge = (g < ng) ? group_at(g) : make_uint2(0u, 0xff800000u);
-          const bool in = g < ng && __uint_as_float(ge.y) >= f2;
-          const unsigned bm = __ballot_sync(FULL, in);
-          if (in && n2 + __popc(bm & ((1u << lane) - 1u)) < kSGroups)
-            gsel[n2 + __popc(bm & ((1u << lane) - 1u))] = static_cast<int>(ge.x);
-          n2 += __popc(bm);
-        }
-        if (lane == 0) {
-          hd.f2 = f2;
-          hd.nlist = 0;
-          hd.cut = n2;  // groups listed (reused as a count here)
-        }
       }
       __syncthreads();
       if (!general) {
-        f = hd.f2;
+        f = f2;
         const int ng2 = (hd.cut <= kSGroups) ? hd.cut : 0;  // more: the general path (no keys)
         const float tf = Seg<E>::grid_floor(f);
         // item = (group, vector of the group); the loads of a round go out together
