@@ -16,19 +16,21 @@
 // spinning).
 //
 //   * spec_stream_kernel, one launch per call: rows whose starts are 16-byte
-//     aligned, greedy or top-k with k <= 64.  A persistent grid of four
-//     128-thread CTAs per SM takes whole rows in order.  Each warp keeps a ring
-//     of bulk-copy buffers full (across row boundaries) and reduces its
-//     stages to a running max and first argmax; top-k also keeps the lane
-//     groups (six 16-byte vectors of a stage) whose max reaches a rising
-//     threshold, since a row's top k elements lie in its k largest groups.
-//     At the row end the largest groups are read back, one warp sorts the
-//     candidates, cuts top-k then top-p, and writes the kept set (index order)
-//     and the row record; the CTA that completes a sequence runs its accept
-//     tests and final draw.  Rows it cannot settle (ties past its buffers,
-//     non-finite values) take the exact general path below.
+//     aligned (ragged batches included), greedy, top-k with k <= 64, or top-p
+//     alone.  A persistent grid of four 128-thread CTAs per SM takes whole
+//     rows in order.  Each warp keeps a ring of bulk-copy buffers full and
+//     reduces its stages to a running max and first argmax; top-k and top-p
+//     also keep the lane groups (six 16-byte vectors of a stage) whose max
+//     reaches a rising threshold, since a row's top k elements lie in its k
+//     largest groups, and top-p sums the normaliser as it streams.  At the
+//     row end the groups that can hold the kept set are read back and ranked
+//     (a warp sort for top-k; a counting cut over the bf16 grid, or a block
+//     sort, for top-p), and the kept set (index order) and the row record are
+//     written; the CTA that completes a sequence runs its accept tests and
+//     final draw.  Rows it cannot settle (ties past its buffers, nuclei longer
+//     than its pool, non-finite values) take the exact general path below.
 //   * spec_seg_kernel + spec_row_kernel, two launches: everything else (no
-//     filter, top-p alone, top-k > 64, unaligned rows).  The segment kernel
+//     filter, top-k > 64, unaligned rows).  The segment kernel
 //     streams 24 KB segments of every row (max, first argmax, the normaliser
 //     where the row needs the full sum, a candidate list above a floor); the
 //     row kernel, a programmatic dependent launch, merges each row's segment
@@ -2511,7 +2513,7 @@ __global__ void __launch_bounds__(kThreads, sizeof(E) == 4 ? 8 : 5) spec_row_ker
 
 // ---------------------------------------------------------------------------
 // The one-launch streaming kernel (rows whose starts are 16-byte aligned;
-// greedy, or top-k with k <= kSK).
+// greedy, top-k with k <= kSK, or top-p alone; ragged batches too).
 //
 // A persistent grid, four CTAs per SM; CTA c takes rows c, c + G, c + 2G, ...
 // in order, so whole sequences complete one after another through the launch
@@ -2536,13 +2538,20 @@ __global__ void __launch_bounds__(kThreads, sizeof(E) == 4 ? 8 : 5) spec_row_ker
 //     buffered group max whenever the buffer passes a high-water mark; every
 //     such value bounds the row's k-th element from below, so a warp also
 //     takes any higher value another warp publishes.
-//   * Row end: the k-th largest group max over the whole row, f2; the groups
-//     at or above it are read back from the row (one round of loads), their
-//     elements >= f2 ranked by one warp in registers (value desc, index asc);
-//     the first k, then the top-p prefix within them, are the kept set,
-//     written in index order with the row record.  Ties or a buffer too small
-//     for a stage send the row to the exact general path.  The CTA that
-//     completes a sequence (a counter) runs its accept tests and final draw.
+//   * Row end: the k-th largest group max over the whole row, f2 (a radix
+//     select over every buffered group); the groups at or above it are read
+//     back from the row (one round of loads), their elements >= f2 ranked by
+//     one warp in registers (value desc, index asc); the first k, then the
+//     top-p prefix within them, are the kept set, written in index order with
+//     the row record.  Ties or a buffer too small for a stage send the row to
+//     the exact general path.  The CTA that completes a sequence (a counter)
+//     runs its accept tests and final draw.
+//   * Top-p alone: each lane also sums its groups' weights (the normaliser),
+//     and the warps keep their 160 largest groups.  At the row end f2 is the
+//     largest group max whose groups' maxima alone weigh top_p * Z; the
+//     elements >= f2 of those groups form a pool in the drained ring (the
+//     issue cursor stops at the row's end in this mode), cut by counting bf16
+//     grid points (else a block sort) and written in index order.
 
 constexpr int kSK = 64;            // largest top-k the streaming kernel collects
 constexpr int kSWV = 192;          // vectors per warp-stage (3 KB)
@@ -2946,10 +2955,15 @@ struct RowRing {
   int my, nw;
   const uint4* src;
 };
-template <typename E, bool RAG>
+// A row of a streaming launch: a ragged call (a per-row table) or not.
+__device__ __forceinline__ RowInfo stream_job(const KArgs& a, int row) {
+  return a.row_map ? decode_job<true>(a, row) : decode_job<false>(a, row);
+}
+
+template <typename E>
 __device__ __noinline__ RowRing row_ring(const KArgs& a, int row, int warp) {
   constexpr int N = Seg<E>::N;
-  const RowInfo ri = decode_job<RAG>(a, row);
+  const RowInfo ri = stream_job(a, row);
   RowRing r;
   const int nv = (a.V + N - 1) / N, nst = (nv + kSWV - 1) / kSWV;
   r.my = (nst > warp) ? (nst - warp + kWarps - 1) / kWarps : 0;
@@ -3105,7 +3119,6 @@ __device__ void stream_epilogue(const KArgs& a, int b, int K, int first, Scratch
 // groups), kSMTopP (candidate groups and the normaliser; top-p alone).
 template <typename E, int MODE>
 __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a) {
-  constexpr bool RAG = false;  // ragged calls take the two-kernel path
   constexpr bool CAND = MODE != kSMGreedy, TOPP = MODE == kSMTopP;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Scratch& sm = *reinterpret_cast<Scratch*>(smem_raw);
@@ -3141,14 +3154,14 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
   int ir = static_cast<int>(blockIdx.x), ik = 0, ib = 0, inflight = 0;
   int ilim = TOPP ? ir : INT_MAX;
   RowRing ig{0, 0, nullptr};
-  if (lane == 0 && ir < a.nrows) ig = row_ring<E, RAG>(a, ir, warp);
+  if (lane == 0 && ir < a.nrows) ig = row_ring<E>(a, ir, warp);
   auto top_up = [&]() {
     while (staged && inflight < kSNS && ir < a.nrows) {
       if (ik >= ig.my) {
         if (ir >= ilim) break;
         ir += G;
         ik = 0;
-        if (ir < a.nrows) ig = row_ring<E, RAG>(a, ir, warp);
+        if (ir < a.nrows) ig = row_ring<E>(a, ir, warp);
         continue;
       }
       const int vs = (warp + kWarps * ik) * kSWV;
@@ -3169,7 +3182,7 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
       ilim = row;
       top_up();
     }
-    const RowInfo ri = decode_job<RAG>(a, row);
+    const RowInfo ri = stream_job(a, row);
     const E* grow = static_cast<const E*>(ri.is_target ? a.tgt : a.drf) + ri.row_off;
     const uint4* gv = reinterpret_cast<const uint4*>(grow);
     const int nst = (nv + kSWV - 1) / kSWV;

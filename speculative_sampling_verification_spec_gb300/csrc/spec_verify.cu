@@ -156,7 +156,7 @@ spec_status set_smem(DevInfo& di, int slot, const void* fn, size_t bytes) {
 }
 
 // The streaming kernel takes greedy, top-k (k <= kSK, with or without top-p)
-// and top-p calls whose rows start on 16-byte boundaries, except ragged ones: a
+// and top-p calls (ragged or not) whose rows start on 16-byte boundaries: a
 // persistent grid, as many CTAs as fit at once, one row at a time each (the row record and the kept list go
 // where the two-kernel path puts them; its per-row part record is written only
 // for the general path).
@@ -164,7 +164,7 @@ spec_status plan_stream(const spec_params* p, DevInfo& di, Plan* pl) {
   const bool use_k = !p->greedy && p->top_k > 0 && p->top_k < p->V;
   const bool use_p = !p->greedy && p->top_p < 1.0f;
   // no filter stays on the two-kernel path (the kept set is the whole row)
-  if (!pl->aligned || pl->ragged) return SPEC_OK;
+  if (!pl->aligned) return SPEC_OK;
   int mode;
   if (p->greedy) mode = kSMGreedy;            // max and argmax
   else if (use_k && p->top_k <= kSK) mode = kSMTopK;  // candidate groups (top-p within them)

@@ -361,7 +361,10 @@ def test_sample_verify_equals_draw_then_verify(sv, name, kw, prm):
     ("c3", dict(B=24, V=30011), {}),
     ("c5", dict(B=12), {}),
     ("c4", dict(B=40, V=20011), {}),
-    ("c1", dict(B=300), dict(top_k=6, top_p=0.85))])
+    ("c1", dict(B=300), dict(top_k=6, top_p=0.85)),
+    # 16-byte aligned rows: the streaming kernel's ragged rows (top-p, greedy)
+    ("c3", dict(B=24, V=32768), {}),
+    ("c4", dict(B=40, V=20000), {})])
 def test_ragged_batch_equals_per_sequence_verify(sv, name, kw, prm):
     """Each sequence of a ragged call gives the oracle's verification with its own
     draft length K_b: the first K_b draft tokens, uniform columns 0..K_b."""
@@ -390,7 +393,7 @@ def test_ragged_batch_equals_per_sequence_verify(sv, name, kw, prm):
 
 
 @pytest.mark.parametrize("name,kw", [("c5", dict(B=6)), ("c4", dict(B=20, V=20011)), ("c3", dict(B=8, V=30011)),
-                                     ("c2", {})])
+                                     ("c2", {}), ("c3", dict(B=8, V=32768)), ("c4", dict(B=20, V=20000))])
 def test_ragged_with_equal_lengths_is_spec_verify(sv, name, kw):
     """A ragged call whose lengths all equal K gives spec_verify's outputs bit for bit."""
     w = workloads.make(name, **kw)
