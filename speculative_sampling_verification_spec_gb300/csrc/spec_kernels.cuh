@@ -713,7 +713,7 @@ __device__ __forceinline__ auto row_loader(const RowCtx<E>& rc) {
 
 // ---- probe pass: counts / masses of elements >= each threshold ----------------
 // thr[0] > thr[1] > ... > thr[np-1]; restricted to `rcut` when `restricted`.
-// Cluster totals are returned in cnt_out / mass_out (all threads).
+// The CTA's totals are returned in cnt_out / mass_out (all threads).
 template <typename E>
 __device__ void probe_pass(const RowCtx<E>& rc, Scratch& sm, Local& C, const float (&thr)[kProbes], int np,
                            bool with_mass, bool restricted, Cut rcut, int (&cnt_out)[kProbes],
@@ -2559,10 +2559,12 @@ constexpr int kSVPL = kSWV / 32;   // vectors per lane and stage
 constexpr int kSNS = 3;            // buffers per warp
 constexpr int kSWCap = 256;        // candidate entries per warp
 constexpr int kSKeys = 256;        // row-end ranking capacity (keys in the Scratch's candidate arrays)
-constexpr int kSGroups = 512;      // row-end groups read back (their first vectors, after the keys)
+constexpr int kSGroups = 512;      // top-k row end: groups read back (their first vectors, after the keys)
 constexpr int kSPKeep = 160;       // top-p: groups a warp keeps when its buffer is cut
 constexpr int kSPHwm = kSWCap - 32; // top-p: buffer entries that trigger the cut (a stage adds <= 32)
 constexpr int kSPBuckets = 2048;   // bf16 top-p pool cut: grid points between the floor and the max
+constexpr int kSPItems = 5120;     // top-p row end: group vectors read back (after the pool and its keys)
+constexpr int kSVShift = 26;       // a buffer entry: first vector of the group | (top-p) its vectors' mask << kSVShift
 constexpr size_t kSStage = static_cast<size_t>(kSWV) * 16;
 constexpr size_t kSRing = static_cast<size_t>(kWarps) * kSNS * kSStage;
 constexpr size_t kSCand = static_cast<size_t>(kWarps) * kSWCap * sizeof(uint2);
@@ -2572,8 +2574,9 @@ static_assert(kListTable <= sizeof(int32_t) * kCap + sizeof(float) * kCap &&
                       sizeof(int32_t) * kCap + sizeof(float) * kCap,
               "the merge's entry table and the row-end keys fit the Scratch's candidate arrays");
 static_assert(kSK <= kSWV && 4 * kSK <= kSWCap && kSK <= 64, "a warp's first stage and buffer hold k candidates");
-static_assert(kPool * (2 * sizeof(int32_t) + sizeof(unsigned long long)) + kWarps * kSWCap * sizeof(int32_t) <= kSRing,
-              "the top-p row end's pool, sort keys and group list fit the drained stage ring");
+static_assert(kPool * (2 * sizeof(int32_t) + sizeof(unsigned long long)) + kSPItems * sizeof(int32_t) <= kSRing,
+              "the top-p row end's pool, sort keys and vector list fit the drained stage ring");
+static_assert(kSVPL <= 32 - kSVShift, "a group's vector mask fits above its first vector");
 static_assert(kSPKeep < kSPHwm, "a cut buffer has room for the next stage");
 static_assert(kSPBuckets * sizeof(int) <= kPool * sizeof(unsigned long long) && kThreads <= kSPBuckets,
               "the bf16 pool cut's buckets (then the bitmap's run prefixes) fit the sort-key space");
@@ -3307,7 +3310,17 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
             if (wn + c > kSWCap) {
               wover = true;  // ties beyond the buffer: the row takes the general path
             } else {
-              if (hot) wc[wn + __popc(hb & ((1u << lane) - 1u))] = make_uint2(static_cast<uint32_t>(vs + lane), __float_as_uint(tm));
+              if (hot) {
+                // top-p: which of the group's vectors reach te (only those can
+                // hold an element >= any later floor)
+                uint32_t vmk = 0;
+                if constexpr (TOPP) {
+#pragma unroll
+                  for (int j = 0; j < kSVPL; ++j) vmk |= (Seg<E>::pw_max(pw[j]) >= te) ? (1u << j) : 0u;
+                }
+                wc[wn + __popc(hb & ((1u << lane) - 1u))] =
+                    make_uint2(static_cast<uint32_t>(vs + lane) | (vmk << kSVShift), __float_as_uint(tm));
+              }
               wn += c;
               __syncwarp();
             }
@@ -3405,22 +3418,30 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
         const float need = zrow.hi * a.top_p * (1.0f + 0x1p-10f);
         f2 = fmaxf(f, key_floor(block_select_mass<PER, KB>(gkey, gw, need, okey32(f), okey32(m), hd.wpart)));
       }
+      // the marked vectors of the groups >= f2, listed
       {
         int cnt = 0;
 #pragma unroll
-        for (int p = 0; p < PER; ++p) cnt += (gkey[p] != 0u && okey32_val(gkey[p]) >= f2) ? 1 : 0;
+        for (int p = 0; p < PER; ++p)
+          if (gkey[p] != 0u && okey32_val(gkey[p]) >= f2) cnt += __popc(wc[p * 32 + lane].x >> kSVShift);
         int pos = warp_reserve(&hd.cut, cnt);
 #pragma unroll
         for (int p = 0; p < PER; ++p)
-          if (gkey[p] != 0u && okey32_val(gkey[p]) >= f2) gsel[pos++] = static_cast<int>(wc[p * 32 + lane].x);
+          if (gkey[p] != 0u && okey32_val(gkey[p]) >= f2) {
+            const uint32_t e = wc[p * 32 + lane].x;
+            const int v0 = static_cast<int>(e & ((1u << kSVShift) - 1u));
+            for (uint32_t b = e >> kSVShift; b; b &= b - 1, ++pos)
+              if (pos < kSPItems) gsel[pos] = v0 + (__ffs(b) - 1) * 32;
+          }
       }
       __syncthreads();
+      general = general || hd.cut > kSPItems;
       if (!general) {
-        const int ng2 = hd.cut;
+        const int ni = hd.cut;
         const float tf = Seg<E>::grid_floor(f2);
         // item = (group, vector of the group); the loads of a round go out together
         constexpr int R = 8;
-        for (int base = 0; base < ng2 * kSVPL; base += R * kThreads) {
+        for (int base = 0; base < ni; base += R * kThreads) {
           uint4 x[R];
           int vv[R];
 #pragma unroll
@@ -3428,9 +3449,8 @@ __global__ void __launch_bounds__(kThreads, 4) spec_stream_kernel(const KArgs a)
             const int it = base + r * kThreads + tid;
             vv[r] = -1;
             x[r] = Seg<E>::neg_inf();
-            if (it < ng2 * kSVPL) {
-              const int g = it / kSVPL, j = it - g * kSVPL;
-              const int v = gsel[g] + j * 32;
+            if (it < ni) {
+              const int v = gsel[it];
               vv[r] = v;
               if (v < nw) x[r] = ld_stream(gv + v);
               else if (v < nv) x[r] = Seg<E>::load_some(grow, v, a.V - v * N);

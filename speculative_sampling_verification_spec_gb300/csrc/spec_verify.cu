@@ -165,6 +165,8 @@ spec_status plan_stream(const spec_params* p, DevInfo& di, Plan* pl) {
   const bool use_p = !p->greedy && p->top_p < 1.0f;
   // no filter stays on the two-kernel path (the kept set is the whole row)
   if (!pl->aligned) return SPEC_OK;
+  // a candidate group's first vector shares its buffer word with the mask of its vectors
+  if ((static_cast<int64_t>(p->V) * pl->esize + 15) / 16 >= (int64_t(1) << kSVShift)) return SPEC_OK;
   int mode;
   if (p->greedy) mode = kSMGreedy;            // max and argmax
   else if (use_k && p->top_k <= kSK) mode = kSMTopK;  // candidate groups (top-p within them)
