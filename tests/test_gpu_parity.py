@@ -143,6 +143,8 @@ def _custom(B, K, V, rng, scale=2.0, dtype="f32"):
     dict(V=4096, K=2, B=6, dtype="bf16", temperature=0.8, top_p=0.9),
     dict(V=12000, K=3, B=5, scale=3.0, top_p=0.7),
     dict(V=8192, K=2, B=4, dtype="bf16", scale=1.0, top_p=0.95),  # nuclei of hundreds of tokens
+    # bf16 nuclei of ~1500 tokens: past the streaming kernel's pool, so the general path
+    dict(V=2048, K=1, B=32, dtype="bf16", top_p=0.9, scale=0.3),
     dict(V=4099, K=3, B=5, dtype="bf16", top_k=13, temperature=0.7),
     dict(V=2048, K=4, B=8, greedy=True, dtype="bf16", scale=0.3),   # many exact ties
 ])
